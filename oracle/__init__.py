@@ -1,0 +1,210 @@
+"""CPU oracle for the fused attention forward -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its binding) never imports, links or executes anything here, and this package
+imports nothing from the product package.
+
+Two independent implementations of the same definition live here:
+
+* ``oracle_fwd`` -- the fp64 C oracle in ``fmha_oracle.c`` (OpenMP over rows),
+  called through ctypes on numpy arrays.  It is the reference the GPU parity
+  tests compare against.
+* ``brute_force_fwd`` -- pure-Python float loops with ``math.exp`` and no max
+  shift, for tiny shapes only.  It exists to pin the C oracle.
+
+The definition both follow (sources: "[BUG] Unexpected Slower Performance in
+C++ CuTe (77_blackwell_fmha) vs Python CuTe DSL (fmha.py) on Jetson Thor",
+section "Implementation Differences in softmax_step"; "[BUG] CuTe DSL 4.7/4.8
+regression: FlashAttention-4 SM100 forward kernel spills registers", section
+"Steps/Code to reproduce bug"): per sequence, head and query row i,
+``s_ij = scale * q_i . k_j`` over the visible keys ``j < Lk`` (and
+``j <= i + Lk - Lq`` when causal), ``O_i = softmax_j(s_ij) @ V`` and
+``LSE_i = log sum_j exp(s_ij)``.  A row with no visible key has O = 0 and
+LSE = -inf.  Readings of points the pages leave open (LSE base, causal
+alignment for Lq != Lk, empty rows) are stated in ``fmha_oracle.c``.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, a library softmax, brute force, structural invariants and
+planted mistakes).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fmha_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the C oracle with gcc + OpenMP into a shared library."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _load(path: str = _LIB_PATH):
+    lib = ctypes.CDLL(path)
+    fn = lib.oracle_fmha_fwd
+    fn.restype = ctypes.c_int
+    fn.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # q k v
+        ctypes.c_void_p, ctypes.c_void_p,  # out lse
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,  # cu_q cu_k batch
+        ctypes.c_int64, ctypes.c_int64,  # total_q total_k
+        ctypes.c_int, ctypes.c_int,  # max_seqlen_q max_seqlen_k
+        ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,  # heads head_dim scale causal
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,  # rows n_rows n_threads
+    ]
+    lib.oracle_num_threads.restype = ctypes.c_int
+    return lib
+
+
+def load_variant(source_text: str, workdir: str):
+    """Compile C source text (a variant of ``fmha_oracle.c``) and load it."""
+    src = os.path.join(workdir, "variant.c")
+    out = os.path.join(workdir, "libvariant.so")
+    with open(src, "w") as f:
+        f.write(source_text)
+    build(force=True, src=src, out=out)
+    return _load(out)
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+def lib():
+    """The loaded oracle library (built on first use)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _load()
+    return _lib
+
+
+def num_threads() -> int:
+    return int(lib().oracle_num_threads())
+
+
+def _bits(a) -> np.ndarray:
+    """bf16 data as a contiguous uint16 numpy array of bit patterns.
+
+    Accepts a numpy uint16 array or a CPU torch bfloat16 tensor.
+    """
+    if isinstance(a, np.ndarray):
+        if a.dtype != np.uint16:
+            raise TypeError("expected uint16 bf16 bit patterns")
+        return np.ascontiguousarray(a)
+    # torch tensor (imported lazily so the oracle does not require torch)
+    import torch
+
+    if a.dtype != torch.bfloat16:
+        raise TypeError("expected a bfloat16 tensor")
+    return a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def oracle_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seqlen_k,
+               scale, causal, rows=None, n_threads: int = 0, lib_handle=None):
+    """fp64 attention forward from the C oracle.
+
+    q: [total_q, heads, head_dim] bf16 (numpy uint16 bits or torch bf16),
+    k, v: [total_k, heads, head_dim].  cu_seqlens_q / cu_seqlens_k: int32
+    prefix offsets of length batch+1, or None for dense batches.
+    rows: optional int64 array of flattened (token * heads + head) indices.
+    lib_handle: a library from ``load_variant`` (tests build deliberately
+    broken copies of the C source to show the pins catch them).
+    Returns (out, lse): full mode out [total_q, heads, head_dim] and lse
+    [heads, total_q]; row mode out [n_rows, head_dim] and lse [n_rows].
+    """
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    if qb.ndim != 3:
+        raise ValueError("q must be [tokens, heads, head_dim]")
+    total_q, heads, head_dim = qb.shape
+    total_k = kb.shape[0]
+    if kb.shape[1:] != (heads, head_dim) or vb.shape != kb.shape:
+        raise ValueError("k and v must be [total_k, heads, head_dim]")
+    if (cu_seqlens_q is None) != (cu_seqlens_k is None):
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both be given or both be None")
+    cu_q = cu_k = None
+    if cu_seqlens_q is not None:
+        cu_q = np.ascontiguousarray(np.asarray(cu_seqlens_q, dtype=np.int32))
+        cu_k = np.ascontiguousarray(np.asarray(cu_seqlens_k, dtype=np.int32))
+        if cu_q.shape != (batch + 1,) or cu_k.shape != (batch + 1,):
+            raise ValueError("cu_seqlens must have batch + 1 entries")
+    if rows is None:
+        out = np.zeros((total_q, heads, head_dim), dtype=np.float64)
+        lse = np.zeros((heads, total_q), dtype=np.float64)
+        rows_arr, n_rows = None, 0
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n_rows = rows_arr.shape[0]
+        out = np.zeros((n_rows, head_dim), dtype=np.float64)
+        lse = np.zeros((n_rows,), dtype=np.float64)
+    handle = lib() if lib_handle is None else lib_handle
+    rc = handle.oracle_fmha_fwd(
+        qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, out.ctypes.data, lse.ctypes.data,
+        cu_q.ctypes.data if cu_q is not None else None,
+        cu_k.ctypes.data if cu_k is not None else None,
+        int(batch), int(total_q), int(total_k), int(max_seqlen_q), int(max_seqlen_k),
+        int(heads), int(head_dim), float(scale), int(bool(causal)),
+        rows_arr.ctypes.data if rows_arr is not None else None, int(n_rows), int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_fmha_fwd rejected its arguments")
+    return out, lse
+
+
+def _bf16_bits_to_float(bits: int) -> float:
+    return float(np.array([bits << 16], dtype=np.uint32).view(np.float32)[0])
+
+
+def brute_force_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seqlen_k,
+                    scale, causal):
+    """Pure-Python float loops, no max shift: exp(s) / sum exp(s) directly.
+
+    Only for tiny shapes with small scores (no overflow).  Same argument
+    conventions and return layout as ``oracle_fwd`` in full mode.
+    """
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    total_q, heads, head_dim = qb.shape
+    to_f = np.vectorize(_bf16_bits_to_float, otypes=[float])
+    Q, K, V = to_f(qb).tolist(), to_f(kb).tolist(), to_f(vb).tolist()
+    out = [[[0.0] * head_dim for _ in range(heads)] for _ in range(total_q)]
+    lse = [[0.0] * total_q for _ in range(heads)]
+    for b in range(batch):
+        if cu_seqlens_q is None:
+            q0, lq, k0, lk = b * max_seqlen_q, max_seqlen_q, b * max_seqlen_k, max_seqlen_k
+        else:
+            q0, lq = int(cu_seqlens_q[b]), int(cu_seqlens_q[b + 1]) - int(cu_seqlens_q[b])
+            k0, lk = int(cu_seqlens_k[b]), int(cu_seqlens_k[b + 1]) - int(cu_seqlens_k[b])
+        for h in range(heads):
+            for i in range(lq):
+                weights = []
+                for j in range(lk):
+                    if causal and j > i + lk - lq:
+                        continue
+                    dot = 0.0
+                    for d in range(head_dim):
+                        dot += Q[q0 + i][h][d] * K[k0 + j][h][d]
+                    weights.append((j, math.exp(scale * dot)))
+                if not weights:
+                    lse[h][q0 + i] = -math.inf
+                    continue
+                z = sum(w for _, w in weights)
+                for d in range(head_dim):
+                    out[q0 + i][h][d] = sum(w * V[k0 + j][h][d] for j, w in weights) / z
+                lse[h][q0 + i] = math.log(z)
+    return np.array(out, dtype=np.float64), np.array(lse, dtype=np.float64)
