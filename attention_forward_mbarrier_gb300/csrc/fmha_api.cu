@@ -1,0 +1,145 @@
+// fmha_api.cu -- host launcher and C ABI of libfmha.so (declared in fmha.h).
+//
+// Validates arguments without touching the GPU, encodes the three TMA tensor
+// maps (Q, K, V viewed as 2-D [tokens, heads * 128] bf16, 64 x 128 boxes with
+// 128-byte swizzle), and launches one CTA per (head, 256-row query block,
+// sequence).  Causal launches walk query blocks from the last to the first so
+// the longest units start first.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fmha.h"
+#include "fmha_fwd_kernel.cuh"
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// [tokens, heads * 128] bf16, row stride heads * 256 bytes, box 64 x 128, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int tokens, int heads) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads) * fmha::kHeadDim, static_cast<cuuint64_t>(tokens)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads) * fmha::kHeadDim * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int configure_kernel() {
+  static int rc = -1;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  // per-process attribute; re-applied cheaply if a previous attempt failed
+  if (rc != 0) {
+    rc = cudaFuncSetAttribute(fmha::fmha_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(fmha::kSmemBytes)) == cudaSuccess
+             ? 0
+             : 1;
+  }
+  return rc;
+}
+
+}  // namespace
+
+extern "C" int fmha_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
+                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int heads,
+                        int head_dim, float scale, int causal, fmha_stream_t stream) {
+  // ---- validation: no GPU work before this point
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return FMHA_ERR_INVALID_ARG;
+  if ((cu_seqlens_q == nullptr) != (cu_seqlens_k == nullptr)) return FMHA_ERR_INVALID_ARG;
+  if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || heads < 1)
+    return FMHA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FMHA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FMHA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      (lse != nullptr && !aligned(lse, 4)))
+    return FMHA_ERR_INVALID_ARG;
+  if (cu_seqlens_q == nullptr) {
+    if (static_cast<int64_t>(batch) * max_seqlen_q != total_q ||
+        static_cast<int64_t>(batch) * max_seqlen_k != total_k)
+      return FMHA_ERR_INVALID_ARG;
+  }
+  if (head_dim != fmha::kHeadDim) return FMHA_ERR_UNSUPPORTED;
+  if (batch > 65535) return FMHA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(heads) * fmha::kHeadDim * 2 >= (int64_t(1) << 32)) return FMHA_ERR_UNSUPPORTED;
+
+  const int pairs = (max_seqlen_q + fmha::kTiles * fmha::kBlockM - 1) / (fmha::kTiles * fmha::kBlockM);
+  if (batch == 0 || total_q == 0 || pairs == 0) return FMHA_OK;  // nothing to compute
+  if (pairs > 65535) return FMHA_ERR_UNSUPPORTED;
+
+  fmha::FwdParams p;
+  // a k/v tensor with no rows still needs a valid map extent; it is never read then
+  const int tk = total_k > 0 ? total_k : 1;
+  if (!make_map(&p.tmap_q, q, total_q, heads) || !make_map(&p.tmap_k, k, tk, heads) ||
+      !make_map(&p.tmap_v, v, tk, heads))
+    return FMHA_ERR_CUDA;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.batch = batch;
+  p.total_q = total_q;
+  p.total_k = total_k;
+  p.max_seqlen_q = max_seqlen_q;
+  p.max_seqlen_k = max_seqlen_k;
+  p.heads = heads;
+  p.causal = causal;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.rescale_threshold = 8.0f;
+
+  if (configure_kernel() != 0) return FMHA_ERR_CUDA;
+  dim3 grid(static_cast<unsigned>(heads), static_cast<unsigned>(pairs), static_cast<unsigned>(batch));
+  fmha::fmha_fwd_kernel<<<grid, fmha::kThreads, fmha::kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
+}
+
+extern "C" int fmha_get_device_status(fmha_stream_t stream, int* detail) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FMHA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, fmha::g_status, sizeof(int)) != cudaSuccess) return FMHA_ERR_CUDA;
+  if (word == 0) {
+    if (detail) *detail = 0;
+    return FMHA_OK;
+  }
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(fmha::g_status, &zero, sizeof(int)) != cudaSuccess) return FMHA_ERR_CUDA;
+  if (detail) *detail = word - 1;
+  return FMHA_ERR_TIMEOUT;
+}
+
+extern "C" const char* fmha_status_string(int status) {
+  switch (status) {
+    case FMHA_OK: return "ok";
+    case FMHA_ERR_INVALID_ARG: return "invalid argument";
+    case FMHA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FMHA_ERR_CUDA: return "CUDA error";
+    case FMHA_ERR_TIMEOUT: return "device pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int fmha_version(void) { return 100; }

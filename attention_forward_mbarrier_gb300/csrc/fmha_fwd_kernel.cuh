@@ -1,0 +1,542 @@
+// fmha_fwd_kernel.cuh -- fused attention forward for sm_103a.
+//
+// O = softmax(scale * Q K^T [+ causal mask]) V and the per-row log-sum-exp, for
+// bf16 [tokens, heads, 128] tensors, dense or varlen (cu_seqlens), after
+// "[BUG] Unexpected Slower Performance in C++ CuTe (77_blackwell_fmha) vs
+// Python CuTe DSL (fmha.py) on Jetson Thor" (sections "Test Commands" and
+// "Implementation Differences in softmax_step") and "[BUG] CuTe DSL 4.7/4.8
+// regression: FlashAttention-4 SM100 forward kernel spills registers"
+// (section "Steps/Code to reproduce bug": varlen causal forward, 512 threads
+// per CTA at a 128-register entry budget).
+//
+// One CTA owns a work unit (sequence b, head h, 256 query rows = two 128-row
+// tiles) and walks the unit's 128-key blocks.  Warp roles (512 threads):
+//   warpgroup 0, 1  softmax for tile 0 / tile 1: tcgen05.ld the S row, track
+//                   the running max, fold scale and -max into one packed FMA,
+//                   ex2, row sum, convert P to bf16 and tcgen05.st it over S;
+//   warpgroup 2     correction: rescales the O accumulator in TMEM when a row
+//                   max moved, and the epilogue (O / l -> bf16 global);
+//   warp 12         TMA producer: Q tiles once, then a K/V ring in shared
+//                   memory gated by full/empty mbarriers;
+//   warp 13         MMA issuer: tcgen05.mma S = Q K^T (both operands in
+//                   shared memory) and O += P V (P from TMEM), completion
+//                   signalled with tcgen05.commit on mbarriers.
+// Tensor memory (512 columns): S0/P0 [0,128), S1/P1 [128,256), O0 [256,384),
+// O1 [384,512).  P (bf16 pairs) overwrites the first 64 columns of its S.
+//
+// Every mbarrier wait is bounded in time: on expiry the kernel records an
+// error word, raises a CTA-wide abort flag, lets in-flight copies and MMAs
+// drain (again bounded), frees its tensor memory and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "sm103_ptx.cuh"
+
+namespace fmha {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlockM = 128;   // query rows per tile (MMA M)
+constexpr int kBlockN = 128;   // keys per block (MMA N of QK^T, K of PV)
+constexpr int kTiles = 2;      // query tiles per CTA
+constexpr int kStages = 4;     // K/V ring slots (each holds one K or one V block)
+constexpr int kThreads = 512;
+constexpr uint32_t kTileBytes = kBlockM * kHeadDim * 2;  // 32 KiB bf16 tile
+constexpr uint32_t kHalfBytes = kTileBytes / 2;          // 64 columns x 128 rows
+constexpr uint32_t kTmemCols = 512;
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffKV = kOffQ + kTiles * kTileBytes;
+constexpr uint32_t kOffBar = kOffKV + kStages * kTileBytes;
+constexpr uint32_t kNumBars = 21;
+constexpr uint32_t kOffMisc = kOffBar + 256;   // tmem base slot, abort flag
+constexpr uint32_t kOffAlpha = kOffBar + 512;  // float [2][128]
+constexpr uint32_t kOffL = kOffAlpha + 1024;   // float [2][128]
+constexpr uint32_t kSmemUsed = kOffL + 1024;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
+static_assert(kNumBars * 8 <= 256, "barrier area");
+
+// barrier ids
+constexpr int kBarQFull = 0;      // [2]
+constexpr int kBarKVFull = 2;     // [kStages]
+constexpr int kBarKVEmpty = 6;    // [kStages]
+constexpr int kBarSFull = 10;     // [2]  QK^T of tile t landed in TMEM
+constexpr int kBarPVReady = 12;   // [2]  P stored and O corrected for tile t
+constexpr int kBarAlpha = 14;     // [2]  softmax published this block's alpha
+constexpr int kBarOFinal = 16;    // [2]  last PV of tile t complete
+constexpr int kBarMmaDone = 18;
+constexpr int kBarLReady = 19;    // [2]  softmax published the final row sum l
+static_assert(kBarKVEmpty == kBarKVFull + kStages && kBarSFull == kBarKVEmpty + kStages, "ids");
+
+// roles, for the timeout detail word
+constexpr int kRoleSoftmax = 1, kRoleCorrection = 2, kRoleLoad = 3, kRoleMma = 4, kRoleDrain = 5;
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
+
+// Register budgets per warpgroup after the split (sum x 128 threads = 64K).
+// Helper calls in these regions must be inlined: ptxas cannot place an ABI
+// call inside a setmaxnreg region.
+constexpr int kRegsSoftmax = 184, kRegsCorrection = 80, kRegsControl = 64;
+static_assert(2 * kRegsSoftmax + kRegsCorrection + kRegsControl == 512, "register split");
+
+struct alignas(64) FwdParams {
+  CUtensorMap tmap_q;  // [total_q, heads*128] bf16, box 64 x 128, 128B swizzle
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
+  __nv_bfloat16* out;
+  float* lse;  // [heads, total_q] or nullptr
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int batch, total_q, total_k, max_seqlen_q, max_seqlen_k, heads;
+  int causal;
+  float scale_log2;         // scale * log2(e)
+  float rescale_threshold;  // skip the O rescale while the max grew by <= this (log2 units)
+};
+
+__device__ int g_status;  // 0 = ok, else 1 + (role * 256 + barrier id) of the first expired wait
+
+struct Ctx {
+  uint32_t bar0;                  // shared address of barrier 0
+  volatile uint32_t* abort_flag;  // shared
+  __device__ __forceinline__ uint32_t bar(int id) const { return bar0 + 8u * id; }
+};
+
+// Wait for the phase of `bar` with the given parity; false on abort or expiry.
+__device__ __forceinline__ bool wait_slow(const Ctx& c, uint32_t bar, uint32_t parity, int code) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*c.abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      *c.abort_flag = 1u;
+      atomicCAS(&g_status, 0, 1 + code);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bar(const Ctx& c, int id, uint32_t parity, int role) {
+  const uint32_t b = c.bar(id);
+  if (ptx::mbar_try_wait(b, parity)) return true;
+  return wait_slow(c, b, parity, role * 256 + id);
+}
+
+// Whole-warp wait: every lane polls, and the warp agrees on the outcome so
+// that the .sync.aligned tcgen05 ops and warp votes after it stay convergent.
+__device__ __forceinline__ bool wait_bar_warp(const Ctx& c, int id, uint32_t parity, int role) {
+  return __all_sync(0xffffffffu, wait_bar(c, id, parity, role));
+}
+
+// Drain wait used on the way out: ignores the abort flag, still bounded.
+__device__ __forceinline__ void wait_drain(const Ctx& c, int id, uint32_t parity) {
+  const uint32_t b = c.bar(id);
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(b, parity)) {
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(&g_status, 0, 1 + kRoleDrain * 256 + id);
+      return;
+    }
+  }
+}
+
+// Key blocks a 128-row query tile starting at sequence row r0 must visit; 0 if
+// the tile is past the sequence end or every row is fully masked.  Causal
+// rows see keys j <= i + (lk - lq).
+__device__ __forceinline__ int tile_blocks(int r0, int lq, int lk, int causal) {
+  if (r0 >= lq) return 0;
+  if (!causal) return (lk + kBlockN - 1) / kBlockN;
+  const int last = min(r0 + kBlockM - 1, lq - 1);
+  const int lim = min(last + lk - lq, lk - 1);
+  return lim >= 0 ? lim / kBlockN + 1 : 0;
+}
+
+__device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
+__device__ __forceinline__ uint32_t col_o(int t) { return 256u + 128u * t; }
+
+// ---------------------------------------------------------------------------
+// MMA issue helpers (one thread)
+// S_t = Q_t K^T: M=128 queries, N=128 keys, K=128 head dims in 8 steps of 16.
+// Q and K tiles are K-major with 128-byte swizzle: two 16 KiB halves (head dims
+// 0..63 and 64..127), rows 128 bytes apart, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ void issue_qk(uint32_t tmem_d, uint32_t q_addr, uint32_t k_addr) {
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, kBlockN, false, false);
+#pragma unroll
+  for (int k = 0; k < kHeadDim / 16; ++k) {
+    const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32u;
+    ptx::mma_ss(tmem_d, ptx::smem_desc_sw128(q_addr + off, 16, 1024),
+                ptx::smem_desc_sw128(k_addr + off, 16, 1024), idesc, k > 0 ? 1u : 0u);
+  }
+}
+
+// O_t (+)= P_t V: M=128 queries, N=128 head dims, K=128 keys in 8 steps of 16.
+// P comes from TMEM (8 columns of bf16 pairs per step); V is MN-major in the
+// same swizzled layout as K: head dims contiguous within a 128-byte row, the
+// second 64 head dims 16 KiB further (leading offset), 8-key groups 1024
+// bytes apart (stride offset), 16 keys = 2048 bytes per step.
+__device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint32_t v_addr,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, kHeadDim, false, true);
+#pragma unroll
+  for (int k = 0; k < kBlockN / 16; ++k) {
+    ptx::mma_ts(tmem_d, tmem_p + 8u * k, ptx::smem_desc_sw128(v_addr + 2048u * k, kHalfBytes, 1024),
+                idesc, (accumulate || k > 0) ? 1u : 0u);
+  }
+}
+
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_constant__ FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_addr);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit: head, 256-row query block, sequence
+  const int h = blockIdx.x;
+  const int pair = p.causal ? static_cast<int>(gridDim.y - 1 - blockIdx.y) : static_cast<int>(blockIdx.y);
+  const int b = blockIdx.z;
+  int q0, lq, k0, lk;
+  if (p.cu_q != nullptr) {
+    q0 = p.cu_q[b];
+    lq = p.cu_q[b + 1] - q0;
+    k0 = p.cu_k[b];
+    lk = p.cu_k[b + 1] - k0;
+  } else {
+    q0 = b * p.max_seqlen_q;
+    lq = p.max_seqlen_q;
+    k0 = b * p.max_seqlen_k;
+    lk = p.max_seqlen_k;
+  }
+  if (lk < 0) lk = 0;
+  const int m0 = pair * (kTiles * kBlockM);
+  if (m0 >= lq) return;  // uniform across the CTA, before any shared state
+
+  // key blocks per tile; causal rows see keys j <= i + (lk - lq)
+  const int off = lk - lq;
+  const int n_blk0 = tile_blocks(m0, lq, lk, p.causal);
+  const int n_blk1 = tile_blocks(m0 + kBlockM, lq, lk, p.causal);
+  const bool active1 = m0 + kBlockM < lq;  // tile 0 is active whenever the unit exists
+  const int n_kv = max(n_blk0, n_blk1);
+  auto n_blk = [&](int t) { return t ? n_blk1 : n_blk0; };
+  auto active = [&](int t) { return t ? active1 : true; };
+
+  Ctx ctx;
+  ctx.bar0 = base + kOffBar;
+  ctx.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  float* s_alpha = reinterpret_cast<float*>(smem + kOffAlpha);
+  float* s_l = reinterpret_cast<float*>(smem + kOffL);
+
+  if (warp == 12 && lane == 0) {
+    for (int t = 0; t < kTiles; ++t) {
+      ptx::mbar_init(ctx.bar(kBarQFull + t), 1);
+      ptx::mbar_init(ctx.bar(kBarSFull + t), 1);
+      ptx::mbar_init(ctx.bar(kBarPVReady + t), 8);  // 4 softmax warps + 4 correction warps
+      ptx::mbar_init(ctx.bar(kBarAlpha + t), 4);    // 4 softmax warps
+      ptx::mbar_init(ctx.bar(kBarOFinal + t), 1);
+      ptx::mbar_init(ctx.bar(kBarLReady + t), 4);  // 4 softmax warps
+    }
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(ctx.bar(kBarKVFull + s), 1);
+      ptx::mbar_init(ctx.bar(kBarKVEmpty + s), 1);
+    }
+    ptx::mbar_init(ctx.bar(kBarMmaDone), 1);
+    *ctx.abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 13) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int wg = warp >> 2;
+  if (wg < 2) {
+    // =============================== softmax (tile t = wg)
+    ptx::setmaxnreg_inc<kRegsSoftmax>();
+    const int t = wg;
+    const int r = (warp & 3) * 32 + lane;  // row within the tile == TMEM lane
+    const uint32_t t_s = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16) + col_s(t);
+    const int row = m0 + kBlockM * t + r;  // sequence-local query index
+    const int nb = n_blk(t);
+    const float c = p.scale_log2;
+    const int key_end = p.causal ? min(row + off + 1, lk) : lk;  // this row's visible keys [0, key_end)
+    const int tile_key_end = p.causal ? min(m0 + kBlockM * t + off + 1, lk) : lk;  // the tile's first row
+    float m_used = -INFINITY;
+    float l = 0.f;
+    for (int j = 0; j < nb; ++j) {
+      if (!wait_bar_warp(ctx, kBarSFull + t, j & 1, kRoleSoftmax)) break;
+      ptx::tc_fence_after();
+      float s[128];
+      ptx::tmem_ld128_wait(t_s, s);
+      const int c0 = j * kBlockN;
+      if (tile_key_end - c0 < kBlockN) {  // block crosses the diagonal or the key tail
+        const int lim = key_end - c0;
+#pragma unroll
+        for (int k = 0; k < 128; ++k)
+          if (k >= lim) s[k] = -INFINITY;
+      }
+      float mx[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float a = ptx::fmax3(s[32 * q + 0], s[32 * q + 1], s[32 * q + 2]);
+#pragma unroll
+        for (int k = 3; k < 31; k += 2) a = ptx::fmax3(a, s[32 * q + k], s[32 * q + k + 1]);
+        mx[q] = fmaxf(a, s[32 * q + 31]);
+      }
+      const float m_blk = ptx::fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+      const float m_new = fmaxf(m_used, m_blk);
+      float alpha = 1.f;
+      // rescale only when the max grew by more than the threshold (NaN when both are -inf: skip)
+      if ((m_new - m_used) * c > p.rescale_threshold) {
+        alpha = ptx::ex2_approx((m_used - m_new) * c);  // m_used == -inf gives 0
+        m_used = m_new;
+      }
+      s_alpha[t * 128 + r] = alpha;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarAlpha + t));
+
+      const float neg_mc = (m_used == -INFINITY) ? 0.f : -m_used * c;
+      const float2 c2 = make_float2(c, c);
+      const float2 nm2 = make_float2(neg_mc, neg_mc);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int k = half * 64 + 2 * i;
+          const float2 x = __ffma2_rn(make_float2(s[k], s[k + 1]), c2, nm2);
+          const float p0 = ptx::ex2_approx(x.x);
+          const float p1 = ptx::ex2_approx(x.y);
+          acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
+          pk[i] = ptx::pack_bf16x2(p0, p1);
+        }
+        ptx::tmem_st32(t_s + 32u * half, pk);
+      }
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+      const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 a = __fadd2_rn(a01, a23);
+      l = l * alpha + (a.x + a.y);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVReady + t));
+    }
+    s_l[t * 128 + r] = l;
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarLReady + t));
+    if (p.lse != nullptr && active(t) && row < lq) {
+      const float lse = (l > 0.f) ? (m_used * c + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      p.lse[static_cast<size_t>(h) * p.total_q + q0 + row] = lse;
+    }
+  } else if (wg == 2) {
+    // =============================== correction + epilogue
+    ptx::setmaxnreg_dec<kRegsCorrection>();
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = (static_cast<uint32_t>(warp & 3) * 32u) << 16;
+    bool ok = true;
+    for (int j = 0; j <= n_kv && ok; ++j) {
+#pragma unroll
+      for (int t = 0; t < kTiles; ++t) {
+        if (!ok) break;
+        const uint32_t t_o = tmem + lane_base + col_o(t);
+        if (j < n_blk(t)) {
+          if (!wait_bar_warp(ctx, kBarAlpha + t, j & 1, kRoleCorrection)) {
+            ok = false;
+            break;
+          }
+          const float alpha = s_alpha[t * 128 + r];
+          if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+              float o[32];
+              ptx::tmem_ld32_wait(t_o + 32u * cc, o);
+              uint32_t u[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(o[i] * alpha);
+              ptx::tmem_st32(t_o + 32u * cc, u);
+            }
+            ptx::tmem_wait_st();
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVReady + t));
+        } else if (j == n_blk(t) && active(t)) {
+          const int nb = n_blk(t);
+          if (nb > 0) {
+            if (!wait_bar_warp(ctx, kBarLReady + t, 0, kRoleCorrection) ||
+                !wait_bar_warp(ctx, kBarOFinal + t, 0, kRoleCorrection)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+          }
+          const float l = nb > 0 ? s_l[t * 128 + r] : 0.f;
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          const int row = m0 + kBlockM * t + r;
+          const bool valid = row < lq;
+          __nv_bfloat16* dst =
+              p.out + (static_cast<size_t>(q0 + row) * p.heads + h) * static_cast<size_t>(kHeadDim);
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            float o[32];
+            if (nb > 0) {
+              ptx::tmem_ld32_wait(t_o + 32u * cc, o);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = 0.f;
+            }
+            if (valid) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cc);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                uint4 w;
+                w.x = ptx::pack_bf16x2(o[8 * v4 + 0] * inv, o[8 * v4 + 1] * inv);
+                w.y = ptx::pack_bf16x2(o[8 * v4 + 2] * inv, o[8 * v4 + 3] * inv);
+                w.z = ptx::pack_bf16x2(o[8 * v4 + 4] * inv, o[8 * v4 + 5] * inv);
+                w.w = ptx::pack_bf16x2(o[8 * v4 + 6] * inv, o[8 * v4 + 7] * inv);
+                d4[v4] = w;
+              }
+            }
+          }
+        }
+      }
+    }
+  } else {
+    ptx::setmaxnreg_dec<kRegsControl>();
+    if (warp == 12) {
+      // =============================== TMA producer
+      if (lane == 0) {
+        ptx::prefetch_tensormap(&p.tmap_q);
+        ptx::prefetch_tensormap(&p.tmap_k);
+        ptx::prefetch_tensormap(&p.tmap_v);
+        const uint64_t pol_q = ptx::policy_evict_first();
+        const uint64_t pol_kv = ptx::policy_evict_last();
+        const int xh = h * kHeadDim;
+#pragma unroll
+        for (int t = 0; t < kTiles; ++t) {
+          if (n_blk(t) > 0) {
+            const uint32_t bar = ctx.bar(kBarQFull + t);
+            ptx::mbar_arrive_expect_tx(bar, kTileBytes);
+            const uint32_t dst = base + kOffQ + t * kTileBytes;
+            const int y = q0 + m0 + kBlockM * t;
+            ptx::tma_load_2d(dst, &p.tmap_q, bar, xh, y, pol_q);
+            ptx::tma_load_2d(dst + kHalfBytes, &p.tmap_q, bar, xh + 64, y, pol_q);
+          }
+        }
+        int issued = 0;
+        for (int j = 0; j < n_kv; ++j) {
+          bool stop = false;
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            const int idx = 2 * j + which;
+            const int slot = idx % kStages;
+            const uint32_t ph = (idx / kStages) & 1;
+            if (!wait_bar(ctx, kBarKVEmpty + slot, ph ^ 1u, kRoleLoad)) {
+              stop = true;
+              break;
+            }
+            const uint32_t bar = ctx.bar(kBarKVFull + slot);
+            ptx::mbar_arrive_expect_tx(bar, kTileBytes);
+            const uint32_t dst = base + kOffKV + slot * kTileBytes;
+            const CUtensorMap* m = which ? &p.tmap_v : &p.tmap_k;
+            const int y = k0 + kBlockN * j;
+            ptx::tma_load_2d(dst, m, bar, xh, y, pol_kv);
+            ptx::tma_load_2d(dst + kHalfBytes, m, bar, xh + 64, y, pol_kv);
+            ++issued;
+          }
+          if (stop) break;
+        }
+        // every issued copy has landed before the CTA may exit
+        for (int idx = max(0, issued - kStages); idx < issued; ++idx)
+          wait_drain(ctx, kBarKVFull + idx % kStages, (idx / kStages) & 1);
+#pragma unroll
+        for (int t = 0; t < kTiles; ++t)
+          if (n_blk(t) > 0) wait_drain(ctx, kBarQFull + t, 0);
+      }
+      __syncwarp();
+    } else if (warp == 13) {
+      // =============================== MMA issuer
+      if (lane == 0) {
+        bool issued_any = false;
+        bool ok = true;
+#pragma unroll
+        for (int t = 0; t < kTiles; ++t)
+          if (ok && n_blk(t) > 0) ok = wait_bar(ctx, kBarQFull + t, 0, kRoleMma);
+        if (ok && n_kv > 0) ok = wait_bar(ctx, kBarKVFull + 0, 0, kRoleMma);
+        if (ok && n_kv > 0) {
+          ptx::tc_fence_after();
+          const uint32_t k_addr = base + kOffKV;
+#pragma unroll
+          for (int t = 0; t < kTiles; ++t) {
+            if (n_blk(t) > 0) {
+              issue_qk(tmem + col_s(t), base + kOffQ + t * kTileBytes, k_addr);
+              ptx::mma_commit(ctx.bar(kBarSFull + t));
+            }
+          }
+          ptx::mma_commit(ctx.bar(kBarKVEmpty + 0));
+          issued_any = true;
+          for (int j = 0; j < n_kv && ok; ++j) {
+            const int vidx = 2 * j + 1, vslot = vidx % kStages;
+            if (!wait_bar(ctx, kBarKVFull + vslot, (vidx / kStages) & 1, kRoleMma)) break;
+            ptx::tc_fence_after();
+            const int kidx = 2 * j + 2, kslot = kidx % kStages;
+            bool k_ready = false;
+#pragma unroll
+            for (int t = 0; t < kTiles; ++t) {
+              if (!ok || j >= n_blk(t)) continue;
+              if (!wait_bar(ctx, kBarPVReady + t, j & 1, kRoleMma)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              issue_pv(tmem + col_o(t), tmem + col_s(t), base + kOffKV + vslot * kTileBytes, j > 0);
+              if (j + 1 < n_blk(t)) {
+                if (!k_ready) {
+                  if (!wait_bar(ctx, kBarKVFull + kslot, (kidx / kStages) & 1, kRoleMma)) {
+                    ok = false;
+                    break;
+                  }
+                  ptx::tc_fence_after();
+                  k_ready = true;
+                }
+                issue_qk(tmem + col_s(t), base + kOffQ + t * kTileBytes, base + kOffKV + kslot * kTileBytes);
+                ptx::mma_commit(ctx.bar(kBarSFull + t));
+              } else {
+                ptx::mma_commit(ctx.bar(kBarOFinal + t));
+              }
+            }
+            if (!ok) break;
+            ptx::mma_commit(ctx.bar(kBarKVEmpty + vslot));
+            if (k_ready) ptx::mma_commit(ctx.bar(kBarKVEmpty + kslot));
+          }
+        }
+        if (issued_any) {  // all MMAs retired before TMEM is released
+          ptx::mma_commit(ctx.bar(kBarMmaDone));
+          wait_drain(ctx, kBarMmaDone, 0);
+        }
+      }
+      __syncwarp();
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fmha

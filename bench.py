@@ -1,0 +1,374 @@
+#!/usr/bin/env python
+"""Benchmark of the fused attention forward on GB300.
+
+One step = one fmha_fwd launch over the whole workload (every query row of
+every head).  Default workload: dense, batch 1, heads 16, seq 2225,
+head_dim 128, non-causal (the shape of the pages' 77_blackwell_fmha /
+fmha.py comparison).  Inputs are seeded synthetic bf16 N(0, 1) tensors.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--no-cpu-baseline]
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs an independent
+replica of the workload on its own GPU (the forward has no exchange step);
+value = units of all ranks / max-over-ranks time.  --impl reference times the
+CPU oracle (fp64) on a bounded row sample on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from attention_forward_mbarrier_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "FMHA fwd TFLOP/s (bf16, d=128) and % of GB300 dense bf16 tensor peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_forward_mbarrier_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(workload_name)
+    if not rec or rec.get("kernel_sha") != kernel_source_sha():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(w: wl.Workload, inp, budget_s: float = 15.0):
+    """Time the oracle (as it stands) on a bounded seeded row sample; TFLOP/s."""
+    import oracle
+
+    oracle.build()
+    rng = np.random.default_rng(123)
+    # cost of a row ~ its visible keys; start small, grow to the time budget
+    n = 64
+    rows = None
+    elapsed = 0.0
+    while True:
+        toks = rng.integers(0, w.total_q, size=n)
+        hs = rng.integers(0, w.heads, size=n)
+        rows = (toks * w.heads + hs).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.oracle_fwd(*inp.oracle_args(), rows=rows)
+        elapsed = time.perf_counter() - t0
+        if elapsed >= budget_s / 3 or n >= w.total_q * w.heads:
+            break
+        n = int(min(n * max(2.0, budget_s / 3 / max(elapsed, 1e-3)), w.total_q * w.heads))
+    flops = sample_flops(w, rows)
+    return {"value": flops / elapsed / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{len(rows)} random (token, head) rows of {w.name}, fp64, "
+                      f"{elapsed:.1f} s, {flops / 1e9:.2f} algorithmic GFLOP"}
+
+
+def sample_flops(w: wl.Workload, rows: np.ndarray) -> float:
+    """Algorithmic FLOPs of the sampled rows: 4 * head_dim * visible keys per row."""
+    cq, ck = w.cu_seqlens()
+    tok = rows // w.heads
+    b = np.searchsorted(cq, tok, side="right") - 1
+    i = tok - cq[b]
+    lq = np.diff(cq)[b]
+    lk = np.diff(ck)[b]
+    vis = np.minimum(lk, np.maximum(0, i + lk - lq + 1)) if w.causal else lk
+    return float(4.0 * w.head_dim * vis.sum())
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    inp = wl.make_inputs(w, seed=0)
+    for _ in range(args.warmup):
+        pass  # the oracle has no state to warm
+    vals = []
+    base = None
+    for _ in range(args.steps):
+        base = cpu_baseline(w, inp, budget_s=args.ref_budget)
+        vals.append(base["value"])
+    value = statistics.median(vals)
+    base["value"] = value
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "description": w.description, "l2": "n/a (CPU)"},
+            "impl": "reference", "cpu_baseline": base,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, rank, world, local):
+    from attention_forward_mbarrier_gb300 import binding
+    from attention_forward_mbarrier_gb300 import build as _build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    _build.build()
+    binding.lib()
+    dev = torch.device("cuda", local)
+    inp = wl.make_inputs(w, seed=0)
+    q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
+    cq = None if inp.cu_seqlens_q is None else inp.cu_seqlens_q.to(dev)
+    ck = None if inp.cu_seqlens_k is None else inp.cu_seqlens_k.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.heads, w.total_q), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+    flush = in_bytes < 2 * L2_BYTES
+    scratch = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+
+    def launch():
+        st = binding.fmha_fwd(q, k, v, out, lse, cq, ck, w.batch, w.total_q, w.total_k,
+                              w.max_seqlen_q, w.max_seqlen_k, w.heads, w.head_dim, w.softmax_scale,
+                              int(w.causal), stream)
+        if st != binding.FMHA_OK:
+            raise RuntimeError(binding.status_string(st))
+
+    for _ in range(max(3, args.warmup)):
+        if flush:
+            scratch.zero_()
+        launch()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            if flush:
+                scratch.zero_()  # L2 flush, outside the timed events
+            starts[i].record(stream)
+            launch()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        t_wall = time.perf_counter() - t_wall
+    st, detail = binding.fmha_get_device_status(stream)
+    if st != binding.FMHA_OK:
+        raise RuntimeError(f"device status {binding.status_string(st)} detail {detail}")
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.mean(times_ms)
+    ms_max = max_over_ranks(ms, world)
+    flops = w.flops()
+    value = world * flops / (ms_max * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host buffers, copies inside the region
+    hq, hk, hv = (t.pin_memory() for t in (inp.q, inp.k, inp.v))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        st2 = binding.fmha_fwd(dq, dk, dv, out, lse, cq, ck, w.batch, w.total_q, w.total_k,
+                               w.max_seqlen_q, w.max_seqlen_k, w.heads, w.head_dim, w.softmax_scale,
+                               int(w.causal), stream)
+        if st2 != binding.FMHA_OK:
+            raise RuntimeError(binding.status_string(st2))
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+
+    if rank != 0:
+        return
+    pk, pk_src = peaks()
+    peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "heads": w.heads,
+                   "total_q": w.total_q, "max_seqlen": w.max_seqlen_q, "causal": w.causal,
+                   "gflop_per_step": flops / 1e9,
+                   "l2": "flushed between steps" if flush else "inputs larger than L2",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_peak": 100.0 * achieved / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "peak_source": f"bf16_tflops (burst) of {pk_src}",
+                     "traffic": recorded_traffic(w.name)},
+        "e2e": {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "wall_s": t_wall,
+        "kernel_ms": {"mean": ms, "min": min(times_ms), "median": statistics.median(times_ms)},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, budget_s=args.ref_budget)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.C2.name, choices=sorted(wl.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per sample")
+    args = ap.parse_args()
+    w = wl.CONFIGS[args.workload]
+    rank, world, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, w, rank, world)
+        else:
+            run_ours(args, w, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,105 @@
+/*
+ * fmha.h -- C ABI of libfmha.so, a fused multi-head attention forward for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (after "[BUG] Unexpected Slower Performance in C++ CuTe
+ * (77_blackwell_fmha) vs Python CuTe DSL (fmha.py) on Jetson Thor", sections
+ * "Test Commands" and "Implementation Differences in softmax_step", and
+ * "[BUG] CuTe DSL 4.7/4.8 regression: FlashAttention-4 SM100 forward kernel
+ * spills registers", section "Steps/Code to reproduce bug"):
+ *
+ *   for every sequence b, head h and query row i of b:
+ *     s_ij  = scale * q_i . k_j   over keys j of sequence b,
+ *             keys with j >= Lk, or (causal) j > i + Lk - Lq, are masked out
+ *     O_i   = sum_j softmax_j(s_ij) v_j            (bf16 output)
+ *     LSE_i = log(sum_j exp(s_ij))                  (natural log, fp32)
+ *
+ * A row with no visible key (Lk = 0, or causal with i + Lk - Lq < 0) gets
+ * O_i = 0 and LSE_i = -inf.  The causal diagonal is aligned to the
+ * bottom-right corner, which is the usual top-left one when Lq == Lk.
+ *
+ * Threading / ownership: every pointer argument is device memory owned by
+ * the caller.  The library allocates no device memory per call and keeps no
+ * per-call state; calls are asynchronous on `stream` and never synchronise
+ * it.  The host never reads device memory (cu_seqlens are read on the GPU).
+ */
+#ifndef FMHA_H_
+#define FMHA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (0 = the legacy default stream). */
+typedef struct CUstream_st *fmha_stream_t;
+
+enum fmha_status_code {
+    FMHA_OK = 0,
+    FMHA_ERR_INVALID_ARG = 1, /* a null or misaligned pointer, inconsistent sizes */
+    FMHA_ERR_UNSUPPORTED = 2, /* a valid request this build does not handle (head_dim != 128) */
+    FMHA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, tensor map) */
+    FMHA_ERR_TIMEOUT = 4      /* a device-side pipeline wait gave up (see fmha_get_device_status) */
+};
+
+/*
+ * fmha_fwd -- O = softmax(scale * Q K^T [+ causal mask]) V and the per-row LSE.
+ *
+ * q            bf16 [total_q, heads, head_dim], contiguous, 16-byte aligned.
+ * k, v         bf16 [total_k, heads, head_dim], contiguous, 16-byte aligned.
+ * out          bf16 [total_q, heads, head_dim], contiguous, 16-byte aligned.
+ *              Rows of every sequence are written; nothing else is touched.
+ * lse          fp32 [heads, total_q], 4-byte aligned, or NULL (not written).
+ * cu_seqlens_q int32 [batch + 1] device array of prefix offsets into the
+ * cu_seqlens_k token dimension (cu[0] = 0, non-decreasing, cu[batch] =
+ *              total), as in the varlen layout of the page above.  Both NULL
+ *              selects dense batches: sequence b holds rows
+ *              [b * max_seqlen, (b + 1) * max_seqlen) -- the [b, s, h, d]
+ *              layout -- and then total_q == batch * max_seqlen_q and
+ *              total_k == batch * max_seqlen_k are required.
+ * batch        number of sequences (>= 0; <= 65535).
+ * total_q,     token counts of q/out and of k/v.  The library needs them for
+ * total_k      the tensor-map bounds and the LSE layout because it never
+ *              reads cu_seqlens on the host.
+ * max_seqlen_q an upper bound on every sequence's query / key length, as in
+ * max_seqlen_k the page's varlen call (the caller's responsibility; a longer
+ *              sequence is not fully computed).
+ * heads        >= 1.
+ * head_dim     must be 128 (else FMHA_ERR_UNSUPPORTED).
+ * scale        finite softmax scale, e.g. 1/sqrt(128); no default is applied.
+ * causal       0 or 1.
+ * stream       CUDA stream the kernel is enqueued on.
+ *
+ * Returns FMHA_OK once the kernel is enqueued (or when there is no work),
+ * FMHA_ERR_INVALID_ARG / FMHA_ERR_UNSUPPORTED before touching the GPU, or
+ * FMHA_ERR_CUDA if encoding the tensor maps or the launch failed.  A device
+ * pipeline wait that gives up does not fault the GPU: the kernel stops, its
+ * outputs are unspecified, and fmha_get_device_status reports it.
+ */
+int fmha_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+             int batch, int total_q, int total_k,
+             int max_seqlen_q, int max_seqlen_k, int heads, int head_dim,
+             float scale, int causal, fmha_stream_t stream);
+
+/*
+ * fmha_get_device_status -- synchronise `stream`, then read and clear the
+ * device status word of the current device.  Returns FMHA_OK if no kernel
+ * reported a problem since the last call, FMHA_ERR_TIMEOUT if a pipeline wait
+ * gave up (then *detail, if non-NULL, receives which wait: role * 256 +
+ * barrier id), or FMHA_ERR_CUDA if the synchronisation itself failed.
+ */
+int fmha_get_device_status(fmha_stream_t stream, int *detail);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *fmha_status_string(int status);
+
+/* ABI version of this library: major * 10000 + minor * 100 + patch. */
+int fmha_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FMHA_H_ */

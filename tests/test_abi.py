@@ -1,0 +1,95 @@
+"""The C ABI library loads, exports every declared symbol, and validates
+arguments on the host before touching the GPU (no GPU needed here)."""
+import os
+import re
+
+import pytest
+
+from attention_forward_mbarrier_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    txt = open(os.path.join(ROOT, "include", "fmha.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fmha_\w+)\s*\(", txt, flags=re.M)
+
+
+def test_header_declares_binding_symbols():
+    assert sorted(declared_functions()) == sorted(binding.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert binding.status_string(0) == "ok"
+    assert "timed out" in binding.status_string(binding.FMHA_ERR_TIMEOUT)
+    assert binding.status_string(99) == "unknown status"
+    assert binding.fmha_version() >= 100
+
+
+GOOD = dict(q=0x1000, k=0x2000, v=0x3000, out=0x4000, lse=0x5000, cu_seqlens_q=0x6000,
+            cu_seqlens_k=0x7000, batch=2, total_q=300, total_k=300, max_seqlen_q=200,
+            max_seqlen_k=200, heads=4, head_dim=128, scale=0.088, causal=1, stream=0)
+
+
+@pytest.mark.parametrize("change,expected", [
+    (dict(q=0), binding.FMHA_ERR_INVALID_ARG),
+    (dict(out=0), binding.FMHA_ERR_INVALID_ARG),
+    (dict(cu_seqlens_k=0), binding.FMHA_ERR_INVALID_ARG),
+    (dict(q=0x1008), binding.FMHA_ERR_INVALID_ARG),  # not 16-byte aligned
+    (dict(lse=0x5002), binding.FMHA_ERR_INVALID_ARG),
+    (dict(heads=0), binding.FMHA_ERR_INVALID_ARG),
+    (dict(batch=-1), binding.FMHA_ERR_INVALID_ARG),
+    (dict(causal=2), binding.FMHA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.FMHA_ERR_INVALID_ARG),
+    (dict(scale=0.0), binding.FMHA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), binding.FMHA_ERR_INVALID_ARG),
+    (dict(head_dim=64), binding.FMHA_ERR_UNSUPPORTED),
+    (dict(batch=70000), binding.FMHA_ERR_UNSUPPORTED),
+    # dense mode needs total == batch * max_seqlen
+    (dict(cu_seqlens_q=0, cu_seqlens_k=0), binding.FMHA_ERR_INVALID_ARG),
+])
+def test_invalid_arguments_rejected_on_host(lib, change, expected):
+    args = dict(GOOD)
+    args.update(change)
+    assert binding.fmha_fwd(**args) == expected
+
+
+def test_empty_problem_is_ok_without_gpu(lib):
+    args = dict(GOOD)
+    args.update(batch=0, total_q=0, total_k=0, max_seqlen_q=0, max_seqlen_k=0)
+    assert binding.fmha_fwd(**args) == binding.FMHA_OK
+
+
+def test_no_gpu_gives_cuda_error_not_crash(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert binding.fmha_fwd(**GOOD) == binding.FMHA_ERR_CUDA
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(RuntimeError):
+        binding.lib()
+
+
+def test_kernel_has_no_register_spills():
+    rep = build.ptxas_report()
+    m = re.findall(r"(\d+) bytes spill stores, (\d+) bytes spill loads", rep)
+    assert m, rep
+    assert all(a == "0" and b == "0" for a, b in m), rep
+    assert "0 bytes stack frame" in rep
