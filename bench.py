@@ -73,7 +73,7 @@ def recorded_traffic(workload_name: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -89,7 +89,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -227,6 +227,42 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def kernel_only(w: wl.Workload, dev, peak: float, steps: int = 5, warmup: int = 3):
+    """Kernel time of another workload (inputs resident, CUDA events), for context."""
+    from attention_forward_mbarrier_gb300 import binding
+
+    inp = wl.make_inputs(w, seed=0)
+    q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
+    cq = None if inp.cu_seqlens_q is None else inp.cu_seqlens_q.to(dev)
+    ck = None if inp.cu_seqlens_k is None else inp.cu_seqlens_k.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.heads, w.total_q), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+    scratch = torch.empty(L2_BYTES, dtype=torch.float32, device=dev) if in_bytes < 2 * L2_BYTES else None
+    ms = []
+    for i in range(warmup + steps):
+        if scratch is not None:
+            scratch.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        st = binding.fmha_fwd(q, k, v, out, lse, cq, ck, w.batch, w.total_q, w.total_k,
+                              w.max_seqlen_q, w.max_seqlen_k, w.heads, w.head_dim, w.softmax_scale,
+                              int(w.causal), stream)
+        e1.record(stream)
+        if st != binding.FMHA_OK:
+            raise RuntimeError(binding.status_string(st))
+        torch.cuda.synchronize()
+        if i >= warmup:
+            ms.append(e0.elapsed_time(e1))
+    mean = statistics.mean(ms)
+    tf = w.flops() / (mean * 1e-3) / 1e12
+    del q, k, v, out, lse, scratch
+    torch.cuda.empty_cache()
+    return {"tflops": tf, "frac_of_peak": tf / peak, "ms": mean, "gflop": w.flops() / 1e9,
+            "causal": w.causal}
+
+
 def run_ours(args, w, rank, world, local):
     from attention_forward_mbarrier_gb300 import binding
     from attention_forward_mbarrier_gb300 import build as _build
@@ -262,6 +298,15 @@ def run_ours(args, w, rank, world, local):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
+        # keep the GPU busy for ~1 s right before the timed region so the
+        # 100 ms clock samples cover the clocks the timed steps run at
+        t_busy = time.perf_counter()
+        while time.perf_counter() - t_busy < args.clock_window:
+            for _ in range(50):
+                if flush:
+                    scratch.zero_()
+                launch()
+            torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
@@ -341,6 +386,8 @@ def run_ours(args, w, rank, world, local):
         "wall_s": t_wall,
         "kernel_ms": {"mean": ms, "min": min(times_ms), "median": statistics.median(times_ms)},
     }
+    if not args.no_secondary:
+        line["secondary"] = {x: kernel_only(wl.CONFIGS[x], dev, peak) for x in args.secondary.split(",") if x}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp, budget_s=args.ref_budget)
     print(json.dumps(line), flush=True)
@@ -354,6 +401,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=wl.C2.name, choices=sorted(wl.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--secondary", default=",".join([wl.C3.name, wl.C4.name, wl.C5.name]),
+                    help="comma-separated workloads timed kernel-only after the main line")
+    ap.add_argument("--clock-window", type=float, default=1.0,
+                    help="seconds of back-to-back launches before the timed region")
     ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per sample")
     args = ap.parse_args()
     w = wl.CONFIGS[args.workload]
