@@ -143,3 +143,12 @@ extern "C" const char* fmha_status_string(int status) {
 }
 
 extern "C" int fmha_version(void) { return 100; }
+
+#ifdef FMHA_TRACE
+// Trace builds only: point the kernel's trace at a device buffer of
+// (query blocks) x 2048 uint64 slots (see fmha_trace.h), or nullptr to stop.
+extern "C" int fmha_debug_set_trace(void* device_buffer) {
+  unsigned long long* p = static_cast<unsigned long long*>(device_buffer);
+  return cudaMemcpyToSymbol(fmha::g_trace, &p, sizeof(p)) == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
+}
+#endif

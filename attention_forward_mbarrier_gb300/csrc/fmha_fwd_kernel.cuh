@@ -98,6 +98,28 @@ struct alignas(64) FwdParams {
 
 __device__ int g_status;  // 0 = ok, else 1 + (role * 256 + barrier id) of the first expired wait
 
+// Opt-in coarse pipeline trace (build with -DFMHA_TRACE): %clock64 stamps at
+// the hand-off points of each role for the CTAs of head 0, sequence 0, one
+// row of kTraceSlots per query block.  Off by default: each stamp is a
+// side-effecting instruction that blocks some scheduling across it.
+constexpr int kTraceSlots = 2048;
+constexpr int kTrSoftmax = 16;      // + t * 512 + j * 8 + event
+constexpr int kTrMma = 1040;        // + j * 8 + event
+constexpr int kTrCorrection = 1300; // + j * 8 + t * 4 + event
+constexpr int kTrLoad = 1600;       // + ring index
+constexpr int kTrMaxBlocks = 32;
+#ifdef FMHA_TRACE
+__device__ unsigned long long* g_trace;
+#define FMHA_TRACE_AT(slot)                                                                 \
+  do {                                                                                      \
+    if (trace_row != nullptr) trace_row[(slot)] = static_cast<unsigned long long>(clock64()); \
+  } while (0)
+#else
+#define FMHA_TRACE_AT(slot) \
+  do {                      \
+  } while (0)
+#endif
+
 struct Ctx {
   uint32_t bar0;                  // shared address of barrier 0
   volatile uint32_t* abort_flag;  // shared
@@ -257,6 +279,12 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+#ifdef FMHA_TRACE
+  unsigned long long* trace_row = (g_trace != nullptr && blockIdx.x == 0 && blockIdx.z == 0)
+                                      ? g_trace + static_cast<size_t>(blockIdx.y) * kTraceSlots
+                                      : nullptr;
+  if (threadIdx.x == 0) FMHA_TRACE_AT(0);
+#endif
 
   const int wg = warp >> 2;
   if (wg < 2) {
@@ -274,9 +302,12 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     float l = 0.f;
     for (int j = 0; j < nb; ++j) {
       if (!wait_bar_warp(ctx, kBarSFull + t, j & 1, kRoleSoftmax)) break;
+      const bool tr = (r == 0 && j < kTrMaxBlocks);
+      if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 0);
       ptx::tc_fence_after();
       float s[128];
       ptx::tmem_ld128_wait(t_s, s);
+      if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 1);
       const int c0 = j * kBlockN;
       if (tile_key_end - c0 < kBlockN) {  // block crosses the diagonal or the key tail
         const int lim = key_end - c0;
@@ -303,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       s_alpha[t * 128 + r] = alpha;
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarAlpha + t));
+      if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 2);
 
       const float neg_mc = (m_used == -INFINITY) ? 0.f : -m_used * c;
       const float2 c2 = make_float2(c, c);
@@ -327,10 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       const float2 a23 = __fadd2_rn(acc[2], acc[3]);
       const float2 a = __fadd2_rn(a01, a23);
       l = l * alpha + (a.x + a.y);
+      if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 3);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVReady + t));
+      if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 4);
     }
     s_l[t * 128 + r] = l;
     __syncwarp();
@@ -355,6 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
             ok = false;
             break;
           }
+          const bool tr = (r == 0 && j < kTrMaxBlocks);
+          if (tr) FMHA_TRACE_AT(kTrCorrection + j * 8 + t * 4 + 0);
           const float alpha = s_alpha[t * 128 + r];
           if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
             ptx::tc_fence_after();
@@ -372,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVReady + t));
+          if (tr) FMHA_TRACE_AT(kTrCorrection + j * 8 + t * 4 + 1);
         } else if (j == n_blk(t) && active(t)) {
           const int nb = n_blk(t);
           if (nb > 0) {
@@ -447,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
               stop = true;
               break;
             }
+            if (idx < 400) FMHA_TRACE_AT(kTrLoad + idx);
             const uint32_t bar = ctx.bar(kBarKVFull + slot);
             ptx::mbar_arrive_expect_tx(bar, kTileBytes);
             const uint32_t dst = base + kOffKV + slot * kTileBytes;
@@ -490,6 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           for (int j = 0; j < n_kv && ok; ++j) {
             const int vidx = 2 * j + 1, vslot = vidx % kStages;
             if (!wait_bar(ctx, kBarKVFull + vslot, (vidx / kStages) & 1, kRoleMma)) break;
+            const bool tr = j < kTrMaxBlocks;
+            if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 0);
             ptx::tc_fence_after();
             const int kidx = 2 * j + 2, kslot = kidx % kStages;
             bool k_ready = false;
@@ -500,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
                 ok = false;
                 break;
               }
+              if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 1 + 2 * t);
               ptx::tc_fence_after();
               issue_pv(tmem + col_o(t), tmem + col_s(t), base + kOffKV + vslot * kTileBytes, j > 0);
               if (j + 1 < n_blk(t)) {
@@ -516,6 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
               } else {
                 ptx::mma_commit(ctx.bar(kBarOFinal + t));
               }
+              if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 2 + 2 * t);
             }
             if (!ok) break;
             ptx::mma_commit(ctx.bar(kBarKVEmpty + vslot));
@@ -531,6 +573,9 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     }
   }
 
+#ifdef FMHA_TRACE
+  if (warp == 8 && lane == 0) FMHA_TRACE_AT(1);
+#endif
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 13) {

@@ -1,0 +1,247 @@
+// microbench.cu -- instruction throughput probes for the attention kernel's
+// building blocks on sm_103a, after the method of "Kernel Bottleneck Tuning",
+// section "1. Measure instruction throughputs in isolation": 8 independent
+// dependency chains per thread, results fed back so the loop cannot be
+// hoisted, %clock64 around the timed loop with a memory clobber.
+//
+// fmha_microbench_alu(which): 0 ex2.approx.ftz.f32, 1 cvt.rn.bf16x2.f32,
+//   2 fma.rn.f32x2.  512 threads per SM.
+// fmha_microbench_mma(...): back-to-back tcgen05.mma kind::f16 M=128 from
+//   `issuers` warps, each rotating nothing (one accumulator per issuer):
+//   a_tmem   0 = A from shared memory (SS), 1 = A from tensor memory (TS)
+//   b_mn     B stored MN-major (as V in O += P V) instead of K-major
+//   n        64, 128 or 256
+//   uniform  1 = the whole warp runs the loop and one lane issues through a
+//              predicate (warp-uniform operands); 0 = lane 0 inside a branch
+// fmha_microbench_tmem_ld: tcgen05.ld 32x32b.x32 + wait, 4 warps.
+// Each writes the per-CTA cycle count of its timed region to out_cycles
+// (host memory, n_ctas entries) and returns 0, 1 on a bad argument, 2 on a
+// CUDA error, 3 if a completion wait expired (bounded at 1 s).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+
+#include "sm103_ptx.cuh"
+
+namespace {
+
+using namespace fmha;
+
+constexpr int kAluThreads = 512;
+constexpr int kTcThreads = 128;
+// shared memory: zeroed A tile (32 KiB) and B tile (64 KiB), barriers
+constexpr uint32_t kMbA = 0, kMbB = 32768, kMbBar = 32768 + 65536, kMbSmem = kMbBar + 128 + 1024;
+
+__global__ void __launch_bounds__(kAluThreads, 1) alu_probe(int which, int reps, long long* out, float* sink) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = 0.001f * (threadIdx.x + i);
+  float2 w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = make_float2(v[i], v[i] + 1.f);
+  __syncthreads();
+  long long t0, t1;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0)::"memory");
+  if (which == 0) {
+    for (int r = 0; r < reps; ++r) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = ptx::ex2_approx(v[i]) * -0.5f;
+    }
+  } else if (which == 1) {
+    for (int r = 0; r < reps; ++r) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t d = ptx::pack_bf16x2(v[i], v[i]);
+        v[i] = __uint_as_float((d & 0xffff0000u) ^ 0x00800000u);
+      }
+    }
+  } else {
+    const float2 a = make_float2(0.999f, 0.999f), c = make_float2(1e-3f, 1e-3f);
+    for (int r = 0; r < reps; ++r) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = __ffma2_rn(w[i], a, c);
+    }
+  }
+  __syncthreads();
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1)::"memory");
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc += v[i] + w[i].x + w[i].y;
+  sink[blockIdx.x * kAluThreads + threadIdx.x] = acc;
+  if (threadIdx.x == 0) out[blockIdx.x] = t1 - t0;
+}
+
+// Shared set-up of the tensor-core probes: zero the operand tiles, init one
+// barrier per warp, allocate all 512 TMEM columns.
+__device__ __forceinline__ uint32_t tc_setup(uint8_t* smem, uint32_t base) {
+  uint32_t* z = reinterpret_cast<uint32_t*>(smem);
+  for (uint32_t i = threadIdx.x; i < kMbBar / 4; i += kTcThreads) z[i] = 0u;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kMbBar + 64);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 4; ++i) ptx::mbar_init(base + kMbBar + 8u * i, 1);
+    ptx::fence_mbar_init();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // zeros visible to the tensor core
+  if ((threadIdx.x >> 5) == 0) {
+    ptx::tmem_alloc(ptx::smem_addr(tslot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  return *tslot;
+}
+
+__device__ __forceinline__ void tc_teardown(uint32_t tmem) {
+  ptx::tc_fence_before();
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+__device__ __forceinline__ bool bounded_wait(uint32_t bar) {
+  const uint64_t g0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, 0))
+    if (ptx::globaltimer_ns() - g0 > 1000000000ull) return false;
+  return true;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) mma_probe(int a_tmem, int b_mn, int n, int issuers, int uniform,
+                                                           int reps, long long* out, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t tmem = tc_setup(smem, base);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  long long t0 = 0, t1 = 0;
+  const bool issuer_warp = warp < issuers;
+  if (issuer_warp && (uniform || lane == 0)) {
+    const uint32_t leader = lane == 0 ? 1u : 0u;
+    // accumulators: issuer w owns columns [w * n, (w + 1) * n) (below 384);
+    // a TMEM A operand sits at columns [448, 512)
+    const uint32_t d = tmem + static_cast<uint32_t>(warp * n);
+    const uint32_t idesc = ptx::idesc_bf16_f32(128, n, false, b_mn != 0);
+    const uint64_t a0 = ptx::smem_desc_sw128(base + kMbA, 16, 1024);
+    // B: K-major rows of 128 bytes (n rows, 8-row groups 1024 apart, 16 KiB
+    // per 64 K) or MN-major (64-wide atoms 16 KiB apart, 16 K rows per step)
+    const uint64_t b0 = b_mn ? ptx::smem_desc_sw128(base + kMbB, 16384, 1024)
+                             : ptx::smem_desc_sw128(base + kMbB, 16, 1024);
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0)::"memory");
+    for (int r = 0; r < reps; ++r) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint64_t a_off = ((k >> 2) * 16384u + (k & 3) * 32u) >> 4;
+        const uint64_t b_off = b_mn ? ((2048u * k) >> 4) : (((k >> 2) * (n * 128u) + (k & 3) * 32u) >> 4);
+        if (uniform) {
+          if (a_tmem)
+            ptx::mma_ts_leader(d, tmem + 448u + 8u * k, b0 + b_off, idesc, 1u, leader);
+          else
+            ptx::mma_ss_leader(d, a0 + a_off, b0 + b_off, idesc, 1u, leader);
+        } else {
+          if (a_tmem)
+            ptx::mma_ts(d, tmem + 448u + 8u * k, b0 + b_off, idesc, 1u);
+          else
+            ptx::mma_ss(d, a0 + a_off, b0 + b_off, idesc, 1u);
+        }
+      }
+    }
+    const uint32_t bar = base + kMbBar + 8u * warp;
+    if (uniform)
+      ptx::mma_commit_leader(bar, leader);
+    else
+      ptx::mma_commit(bar);
+    if (!bounded_wait(bar)) status[0] = 1;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1)::"memory");
+  }
+  __syncwarp();
+  tc_teardown(tmem);
+  if (threadIdx.x == 0) out[blockIdx.x] = t1 - t0;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) tmem_ld_probe(int reps, long long* out, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t tmem = tc_setup(smem, base);
+  const int warp = threadIdx.x >> 5;
+  const uint32_t ta = tmem + ((static_cast<uint32_t>(warp) * 32u) << 16);
+  float acc = 0.f;
+  long long t0, t1;
+  __syncthreads();
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0)::"memory");
+  for (int r = 0; r < reps; ++r) {
+    float x[32];
+    ptx::tmem_ld32_wait(ta + 32u * (r & 7), x);
+    acc += x[0] + x[17] + x[31];
+  }
+  __syncthreads();
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1)::"memory");
+  if (acc == 12345.f) status[1] = 1;  // keeps the loads
+  tc_teardown(tmem);
+  if (threadIdx.x == 0) out[blockIdx.x] = t1 - t0;
+}
+
+int finish(long long* d_out, int* d_status, float* d_sink, long long* out_cycles, int n_ctas) {
+  int rc = 0;
+  int st[2] = {0, 0};
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) fprintf(stderr, "microbench: %s\n", cudaGetErrorString(e));
+  if (e != cudaSuccess ||
+      cudaMemcpy(out_cycles, d_out, sizeof(long long) * n_ctas, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(st, d_status, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess)
+    rc = 2;
+  else if (st[0] != 0)
+    rc = 3;
+  cudaFree(d_out);
+  cudaFree(d_status);
+  if (d_sink) cudaFree(d_sink);
+  return rc;
+}
+
+bool alloc(long long** d_out, int** d_status, int n_ctas) {
+  if (cudaMalloc(d_out, sizeof(long long) * n_ctas) != cudaSuccess) return false;
+  if (cudaMalloc(d_status, 2 * sizeof(int)) != cudaSuccess) return false;
+  return cudaMemset(*d_status, 0, 2 * sizeof(int)) == cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" int fmha_microbench_alu(int which, int reps, long long* out_cycles, int n_ctas) {
+  if (which < 0 || which > 2 || reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
+  long long* d_out = nullptr;
+  int* d_status = nullptr;
+  float* d_sink = nullptr;
+  if (!alloc(&d_out, &d_status, n_ctas) ||
+      cudaMalloc(&d_sink, sizeof(float) * n_ctas * kAluThreads) != cudaSuccess)
+    return 2;
+  alu_probe<<<n_ctas, kAluThreads>>>(which, reps, d_out, d_sink);
+  return finish(d_out, d_status, d_sink, out_cycles, n_ctas);
+}
+
+extern "C" int fmha_microbench_mma(int a_tmem, int b_mn, int n, int issuers, int uniform, int reps,
+                                   long long* out_cycles, int n_ctas) {
+  if ((n != 64 && n != 128 && n != 256) || issuers < 1 || issuers > 3 || issuers * n > 384 || reps < 1 ||
+      n_ctas < 1 || out_cycles == nullptr || (a_tmem && n != 128))
+    return 1;
+  long long* d_out = nullptr;
+  int* d_status = nullptr;
+  if (!alloc(&d_out, &d_status, n_ctas)) return 2;
+  cudaFuncSetAttribute(mma_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMbSmem));
+  mma_probe<<<n_ctas, kTcThreads, kMbSmem>>>(a_tmem, b_mn, n, issuers, uniform, reps, d_out, d_status);
+  return finish(d_out, d_status, nullptr, out_cycles, n_ctas);
+}
+
+extern "C" int fmha_microbench_tmem_ld(int reps, long long* out_cycles, int n_ctas) {
+  if (reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
+  long long* d_out = nullptr;
+  int* d_status = nullptr;
+  if (!alloc(&d_out, &d_status, n_ctas)) return 2;
+  cudaFuncSetAttribute(tmem_ld_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMbSmem));
+  tmem_ld_probe<<<n_ctas, kTcThreads, kMbSmem>>>(reps, d_out, d_status);
+  return finish(d_out, d_status, nullptr, out_cycles, n_ctas);
+}

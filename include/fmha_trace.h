@@ -1,0 +1,27 @@
+/*
+ * fmha_trace.h -- debug hook of trace builds of libfmha.so (compiled with
+ * -DFMHA_TRACE); the default build does not export it.
+ *
+ * The coarse pipeline trace follows the method of "Kernel Bottleneck Tuning",
+ * section "2. Trace the real pipeline, coarsely": timestamps only at role
+ * hand-off points, so that the instrumented kernel keeps its schedule.
+ */
+#ifndef FMHA_TRACE_H_
+#define FMHA_TRACE_H_
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * fmha_debug_set_trace -- device_buffer: caller-owned device memory of
+ * gridDim.y (query blocks of 256 rows) x 2048 uint64 slots, or NULL.  The
+ * CTAs of head 0 / sequence 0 write %clock64 stamps into row blockIdx.y; the
+ * slot map is the kTr* constants of fmha_fwd_kernel.cuh.  Returns FMHA_OK or
+ * FMHA_ERR_CUDA.
+ */
+int fmha_debug_set_trace(void *device_buffer);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
