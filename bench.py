@@ -49,11 +49,14 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = ("fmha_api.cu", "fmha_fwd_kernel.cuh", "sm103_ptx.cuh")
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_forward_mbarrier_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name in KERNEL_SOURCES:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
