@@ -151,4 +151,10 @@ extern "C" int fmha_debug_set_trace(void* device_buffer) {
   unsigned long long* p = static_cast<unsigned long long*>(device_buffer);
   return cudaMemcpyToSymbol(fmha::g_trace, &p, sizeof(p)) == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
 }
+
+// Trace builds only: per-CTA table of 4 uint64 per CTA (grid size x 4), or nullptr.
+extern "C" int fmha_debug_set_cta_trace(void* device_buffer) {
+  unsigned long long* p = static_cast<unsigned long long*>(device_buffer);
+  return cudaMemcpyToSymbol(fmha::g_trace_ctas, &p, sizeof(p)) == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
+}
 #endif

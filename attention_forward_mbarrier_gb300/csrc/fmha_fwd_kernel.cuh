@@ -54,8 +54,7 @@ constexpr uint32_t kOffBar = kOffKV + kStages * kTileBytes;
 constexpr uint32_t kNumBars = 21;
 constexpr uint32_t kOffMisc = kOffBar + 256;   // tmem base slot, abort flag
 constexpr uint32_t kOffAlpha = kOffBar + 512;  // float [2][128]
-constexpr uint32_t kOffL = kOffAlpha + 1024;   // float [2][128]
-constexpr uint32_t kSmemUsed = kOffL + 1024;
+constexpr uint32_t kSmemUsed = kOffAlpha + 1024;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kNumBars * 8 <= 256, "barrier area");
 
@@ -67,9 +66,17 @@ constexpr int kBarSFull = 10;     // [2]  QK^T of tile t landed in TMEM
 constexpr int kBarPVReady = 12;   // [2]  P stored and O corrected for tile t
 constexpr int kBarAlpha = 14;     // [2]  softmax published this block's alpha
 constexpr int kBarOFinal = 16;    // [2]  last PV of tile t complete
-constexpr int kBarMmaDone = 18;
-constexpr int kBarLReady = 19;    // [2]  softmax published the final row sum l
+constexpr int kBarMmaDone = 18;   // [kIssuers] every MMA of an issuer retired
 static_assert(kBarKVEmpty == kBarKVFull + kStages && kBarSFull == kBarKVEmpty + kStages, "ids");
+
+// MMA issuing warps: 1 = warp 13 issues both tiles in order; 2 = warp 13
+// issues tile 0 and warp 14 tile 1, so a tile's P hand-off never waits behind
+// the other tile's MMA issue.
+#ifndef FMHA_ISSUERS
+#define FMHA_ISSUERS 1
+#endif
+constexpr int kIssuers = FMHA_ISSUERS;
+static_assert(kIssuers == 1 || kIssuers == 2, "MMA issuers");
 
 // roles, for the timeout detail word
 constexpr int kRoleSoftmax = 1, kRoleCorrection = 2, kRoleLoad = 3, kRoleMma = 4, kRoleDrain = 5;
@@ -79,7 +86,7 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 // Register budgets per warpgroup after the split (sum x 128 threads = 64K).
 // Helper calls in these regions must be inlined: ptxas cannot place an ABI
 // call inside a setmaxnreg region.
-constexpr int kRegsSoftmax = 184, kRegsCorrection = 80, kRegsControl = 64;
+constexpr int kRegsSoftmax = 184, kRegsCorrection = 64, kRegsControl = 80;
 static_assert(2 * kRegsSoftmax + kRegsCorrection + kRegsControl == 512, "register split");
 
 struct alignas(64) FwdParams {
@@ -110,6 +117,9 @@ constexpr int kTrLoad = 1600;       // + ring index
 constexpr int kTrMaxBlocks = 32;
 #ifdef FMHA_TRACE
 __device__ unsigned long long* g_trace;
+// per-CTA table (every CTA, linear block id): %globaltimer at entry, after the
+// set-up sync and at exit, and the SM id
+__device__ unsigned long long* g_trace_ctas;
 #define FMHA_TRACE_AT(slot)                                                                 \
   do {                                                                                      \
     if (trace_row != nullptr) trace_row[(slot)] = static_cast<unsigned long long>(clock64()); \
@@ -217,6 +227,15 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+#ifdef FMHA_TRACE
+  const size_t cta_lin = blockIdx.x + static_cast<size_t>(gridDim.x) * (blockIdx.y + static_cast<size_t>(gridDim.y) * blockIdx.z);
+  if (threadIdx.x == 0 && g_trace_ctas != nullptr) {
+    g_trace_ctas[cta_lin * 4 + 0] = ptx::globaltimer_ns();
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    g_trace_ctas[cta_lin * 4 + 3] = smid;
+  }
+#endif
 
   // ---- work unit: head, 256-row query block, sequence
   const int h = blockIdx.x;
@@ -252,7 +271,35 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
   ctx.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   float* s_alpha = reinterpret_cast<float*>(smem + kOffAlpha);
-  float* s_l = reinterpret_cast<float*>(smem + kOffL);
+
+  // TMA producer steps (one thread): the Q tiles, and ring load idx = K (even) or
+  // V (odd) of key block idx / 2 into slot idx % kStages.
+  const int xh = h * kHeadDim;
+  auto load_q = [&](uint64_t pol) {
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+      if (n_blk(t) > 0) {
+        const uint32_t bar = ctx.bar(kBarQFull + t);
+        ptx::mbar_arrive_expect_tx(bar, kTileBytes);
+        const uint32_t dst = base + kOffQ + t * kTileBytes;
+        const int y = q0 + m0 + kBlockM * t;
+        ptx::tma_load_2d(dst, &p.tmap_q, bar, xh, y, pol);
+        ptx::tma_load_2d(dst + kHalfBytes, &p.tmap_q, bar, xh + 64, y, pol);
+      }
+    }
+  };
+  auto load_kv = [&](int idx, uint64_t pol) {
+    const int slot = idx % kStages;
+    const uint32_t bar = ctx.bar(kBarKVFull + slot);
+    ptx::mbar_arrive_expect_tx(bar, kTileBytes);
+    const uint32_t dst = base + kOffKV + slot * kTileBytes;
+    const CUtensorMap* m = (idx & 1) ? &p.tmap_v : &p.tmap_k;
+    const int y = k0 + kBlockN * (idx >> 1);
+    ptx::tma_load_2d(dst, m, bar, xh, y, pol);
+    ptx::tma_load_2d(dst + kHalfBytes, m, bar, xh + 64, y, pol);
+  };
+  // ring loads issued before the CTA-wide set-up sync (the ring starts empty)
+  const int early_loads = min(kStages, 2 * n_kv);
 
   if (warp == 12 && lane == 0) {
     for (int t = 0; t < kTiles; ++t) {
@@ -261,15 +308,21 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       ptx::mbar_init(ctx.bar(kBarPVReady + t), 8);  // 4 softmax warps + 4 correction warps
       ptx::mbar_init(ctx.bar(kBarAlpha + t), 4);    // 4 softmax warps
       ptx::mbar_init(ctx.bar(kBarOFinal + t), 1);
-      ptx::mbar_init(ctx.bar(kBarLReady + t), 4);  // 4 softmax warps
     }
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(ctx.bar(kBarKVFull + s), 1);
-      ptx::mbar_init(ctx.bar(kBarKVEmpty + s), 1);
+      ptx::mbar_init(ctx.bar(kBarKVEmpty + s), kIssuers);  // one release per issuing warp
     }
-    ptx::mbar_init(ctx.bar(kBarMmaDone), 1);
+    for (int i = 0; i < kIssuers; ++i) ptx::mbar_init(ctx.bar(kBarMmaDone + i), 1);
     *ctx.abort_flag = 0u;
     ptx::fence_mbar_init();
+    // start the first copies now: they overlap the TMEM allocation and the sync
+    ptx::prefetch_tensormap(&p.tmap_q);
+    ptx::prefetch_tensormap(&p.tmap_k);
+    ptx::prefetch_tensormap(&p.tmap_v);
+    load_q(ptx::policy_evict_first());
+    const uint64_t pol_kv = ptx::policy_evict_last();
+    for (int idx = 0; idx < early_loads; ++idx) load_kv(idx, pol_kv);
   }
   if (warp == 13) {
     ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
@@ -284,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
                                       ? g_trace + static_cast<size_t>(blockIdx.y) * kTraceSlots
                                       : nullptr;
   if (threadIdx.x == 0) FMHA_TRACE_AT(0);
+  if (threadIdx.x == 0 && g_trace_ctas != nullptr) g_trace_ctas[cta_lin * 4 + 1] = ptx::globaltimer_ns();
 #endif
 
   const int wg = warp >> 2;
@@ -366,20 +420,49 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVReady + t));
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 4);
     }
-    s_l[t * 128 + r] = l;
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarLReady + t));
-    if (p.lse != nullptr && active(t) && row < lq) {
+    // ---- epilogue of this tile: LSE and O / l -> bf16 (rows of the sequence only),
+    // as soon as this tile's last PV completed
+    const bool valid = active(t) && row < lq;
+    if (p.lse != nullptr && valid) {
       const float lse = (l > 0.f) ? (m_used * c + log2f(l)) * 0.69314718055994531f : -INFINITY;
       p.lse[static_cast<size_t>(h) * p.total_q + q0 + row] = lse;
     }
+    if (active(t) && (nb == 0 || wait_bar_warp(ctx, kBarOFinal + t, 0, kRoleSoftmax))) {
+      if (nb > 0) ptx::tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const uint32_t t_o = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16) + col_o(t);
+      __nv_bfloat16* dst =
+          p.out + (static_cast<size_t>(q0 + row) * p.heads + h) * static_cast<size_t>(kHeadDim);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float o[32];
+        if (nb > 0) {
+          ptx::tmem_ld32_wait(t_o + 32u * cc, o);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0.f;
+        }
+        if (valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cc);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 w;
+            w.x = ptx::pack_bf16x2(o[8 * v4 + 0] * inv, o[8 * v4 + 1] * inv);
+            w.y = ptx::pack_bf16x2(o[8 * v4 + 2] * inv, o[8 * v4 + 3] * inv);
+            w.z = ptx::pack_bf16x2(o[8 * v4 + 4] * inv, o[8 * v4 + 5] * inv);
+            w.w = ptx::pack_bf16x2(o[8 * v4 + 6] * inv, o[8 * v4 + 7] * inv);
+            d4[v4] = w;
+          }
+        }
+      }
+    }
   } else if (wg == 2) {
-    // =============================== correction + epilogue
+    // =============================== correction
     ptx::setmaxnreg_dec<kRegsCorrection>();
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (static_cast<uint32_t>(warp & 3) * 32u) << 16;
     bool ok = true;
-    for (int j = 0; j <= n_kv && ok; ++j) {
+    for (int j = 0; j < n_kv && ok; ++j) {
 #pragma unroll
       for (int t = 0; t < kTiles; ++t) {
         if (!ok) break;
@@ -409,92 +492,23 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVReady + t));
           if (tr) FMHA_TRACE_AT(kTrCorrection + j * 8 + t * 4 + 1);
-        } else if (j == n_blk(t) && active(t)) {
-          const int nb = n_blk(t);
-          if (nb > 0) {
-            if (!wait_bar_warp(ctx, kBarLReady + t, 0, kRoleCorrection) ||
-                !wait_bar_warp(ctx, kBarOFinal + t, 0, kRoleCorrection)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-          }
-          const float l = nb > 0 ? s_l[t * 128 + r] : 0.f;
-          const float inv = l > 0.f ? 1.f / l : 0.f;
-          const int row = m0 + kBlockM * t + r;
-          const bool valid = row < lq;
-          __nv_bfloat16* dst =
-              p.out + (static_cast<size_t>(q0 + row) * p.heads + h) * static_cast<size_t>(kHeadDim);
-#pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            float o[32];
-            if (nb > 0) {
-              ptx::tmem_ld32_wait(t_o + 32u * cc, o);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = 0.f;
-            }
-            if (valid) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cc);
-#pragma unroll
-              for (int v4 = 0; v4 < 4; ++v4) {
-                uint4 w;
-                w.x = ptx::pack_bf16x2(o[8 * v4 + 0] * inv, o[8 * v4 + 1] * inv);
-                w.y = ptx::pack_bf16x2(o[8 * v4 + 2] * inv, o[8 * v4 + 3] * inv);
-                w.z = ptx::pack_bf16x2(o[8 * v4 + 4] * inv, o[8 * v4 + 5] * inv);
-                w.w = ptx::pack_bf16x2(o[8 * v4 + 6] * inv, o[8 * v4 + 7] * inv);
-                d4[v4] = w;
-              }
-            }
-          }
         }
       }
     }
   } else {
     ptx::setmaxnreg_dec<kRegsControl>();
     if (warp == 12) {
-      // =============================== TMA producer
+      // =============================== TMA producer (continues after the early loads)
       if (lane == 0) {
-        ptx::prefetch_tensormap(&p.tmap_q);
-        ptx::prefetch_tensormap(&p.tmap_k);
-        ptx::prefetch_tensormap(&p.tmap_v);
-        const uint64_t pol_q = ptx::policy_evict_first();
         const uint64_t pol_kv = ptx::policy_evict_last();
-        const int xh = h * kHeadDim;
-#pragma unroll
-        for (int t = 0; t < kTiles; ++t) {
-          if (n_blk(t) > 0) {
-            const uint32_t bar = ctx.bar(kBarQFull + t);
-            ptx::mbar_arrive_expect_tx(bar, kTileBytes);
-            const uint32_t dst = base + kOffQ + t * kTileBytes;
-            const int y = q0 + m0 + kBlockM * t;
-            ptx::tma_load_2d(dst, &p.tmap_q, bar, xh, y, pol_q);
-            ptx::tma_load_2d(dst + kHalfBytes, &p.tmap_q, bar, xh + 64, y, pol_q);
-          }
-        }
-        int issued = 0;
-        for (int j = 0; j < n_kv; ++j) {
-          bool stop = false;
-#pragma unroll
-          for (int which = 0; which < 2; ++which) {
-            const int idx = 2 * j + which;
-            const int slot = idx % kStages;
-            const uint32_t ph = (idx / kStages) & 1;
-            if (!wait_bar(ctx, kBarKVEmpty + slot, ph ^ 1u, kRoleLoad)) {
-              stop = true;
-              break;
-            }
-            if (idx < 400) FMHA_TRACE_AT(kTrLoad + idx);
-            const uint32_t bar = ctx.bar(kBarKVFull + slot);
-            ptx::mbar_arrive_expect_tx(bar, kTileBytes);
-            const uint32_t dst = base + kOffKV + slot * kTileBytes;
-            const CUtensorMap* m = which ? &p.tmap_v : &p.tmap_k;
-            const int y = k0 + kBlockN * j;
-            ptx::tma_load_2d(dst, m, bar, xh, y, pol_kv);
-            ptx::tma_load_2d(dst + kHalfBytes, m, bar, xh + 64, y, pol_kv);
-            ++issued;
-          }
-          if (stop) break;
+        int issued = early_loads;
+        for (int idx = early_loads; idx < 2 * n_kv; ++idx) {
+          const int slot = idx % kStages;
+          const uint32_t ph = (idx / kStages) & 1;
+          if (!wait_bar(ctx, kBarKVEmpty + slot, ph ^ 1u, kRoleLoad)) break;
+          if (idx < 400) FMHA_TRACE_AT(kTrLoad + idx);
+          load_kv(idx, pol_kv);
+          ++issued;
         }
         // every issued copy has landed before the CTA may exit
         for (int idx = max(0, issued - kStages); idx < issued; ++idx)
@@ -504,7 +518,65 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           if (n_blk(t) > 0) wait_drain(ctx, kBarQFull + t, 0);
       }
       __syncwarp();
-    } else if (warp == 13) {
+    } else if (kIssuers == 2 && (warp == 13 || warp == 14)) {
+      // =============================== MMA issuer of one tile (t = warp - 13)
+      const int t = warp - 13;
+      if (lane == 0) {
+        const int nb = n_blk(t);
+        const uint32_t q_addr = base + kOffQ + t * kTileBytes;
+        bool ok = true, issued_any = false;
+        if (nb > 0) {
+          ok = wait_bar(ctx, kBarQFull + t, 0, kRoleMma) && wait_bar(ctx, kBarKVFull + 0, 0, kRoleMma);
+          if (ok) {
+            ptx::tc_fence_after();
+            issue_qk(tmem + col_s(t), q_addr, base + kOffKV);
+            ptx::mma_commit(ctx.bar(kBarSFull + t));
+            ptx::mma_commit(ctx.bar(kBarKVEmpty + 0));
+            issued_any = true;
+          }
+        }
+        for (int j = 0; j < nb && ok; ++j) {
+          const int vidx = 2 * j + 1, vslot = vidx % kStages;
+          if (!wait_bar(ctx, kBarKVFull + vslot, (vidx / kStages) & 1, kRoleMma) ||
+              !wait_bar(ctx, kBarPVReady + t, j & 1, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          const bool tr = j < kTrMaxBlocks;
+          if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 1 + 2 * t);
+          ptx::tc_fence_after();
+          issue_pv(tmem + col_o(t), tmem + col_s(t), base + kOffKV + vslot * kTileBytes, j > 0);
+          ptx::mma_commit(ctx.bar(kBarKVEmpty + vslot));
+          if (j + 1 < nb) {
+            const int kidx = 2 * j + 2, kslot = kidx % kStages;
+            if (!wait_bar(ctx, kBarKVFull + kslot, (kidx / kStages) & 1, kRoleMma)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            issue_qk(tmem + col_s(t), q_addr, base + kOffKV + kslot * kTileBytes);
+            ptx::mma_commit(ctx.bar(kBarSFull + t));
+            ptx::mma_commit(ctx.bar(kBarKVEmpty + kslot));
+          } else {
+            ptx::mma_commit(ctx.bar(kBarOFinal + t));
+          }
+          if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 2 + 2 * t);
+        }
+        // K/V blocks loaded only for the other tile: release their slots
+        // unused, each after its copy landed (so the arrival counts toward
+        // that use of the slot)
+        for (int idx = 2 * nb; ok && idx < 2 * n_kv; ++idx) {
+          const int slot = idx % kStages;
+          if (!wait_bar(ctx, kBarKVFull + slot, (idx / kStages) & 1, kRoleMma)) break;
+          ptx::mbar_arrive(ctx.bar(kBarKVEmpty + slot));
+        }
+        if (issued_any) {  // all MMAs retired before TMEM is released
+          ptx::mma_commit(ctx.bar(kBarMmaDone + t));
+          wait_drain(ctx, kBarMmaDone + t, 0);
+        }
+      }
+      __syncwarp();
+    } else if (kIssuers == 1 && warp == 13) {
       // =============================== MMA issuer
       if (lane == 0) {
         bool issued_any = false;
@@ -581,6 +653,9 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
   if (warp == 13) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
+#ifdef FMHA_TRACE
+    if (lane == 0 && g_trace_ctas != nullptr) g_trace_ctas[cta_lin * 4 + 2] = ptx::globaltimer_ns();
+#endif
   }
 }
 

@@ -109,8 +109,8 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar) {
   return true;
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) mma_probe(int a_tmem, int b_mn, int n, int issuers, int uniform,
-                                                           int reps, long long* out, int* status) {
+template <int a_tmem, int b_mn, int n, int uniform>
+__global__ void __launch_bounds__(kTcThreads, 1) mma_probe(int issuers, int reps, long long* out, int* status) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -231,8 +231,28 @@ extern "C" int fmha_microbench_mma(int a_tmem, int b_mn, int n, int issuers, int
   long long* d_out = nullptr;
   int* d_status = nullptr;
   if (!alloc(&d_out, &d_status, n_ctas)) return 2;
-  cudaFuncSetAttribute(mma_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMbSmem));
-  mma_probe<<<n_ctas, kTcThreads, kMbSmem>>>(a_tmem, b_mn, n, issuers, uniform, reps, d_out, d_status);
+  // operand arrangement fixed at compile time, so the loop holds only the MMAs
+  auto launch = [&](auto kernel) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMbSmem));
+    kernel<<<n_ctas, kTcThreads, kMbSmem>>>(issuers, reps, d_out, d_status);
+  };
+  const int key = (a_tmem ? 1 : 0) | (b_mn ? 2 : 0) | (uniform ? 4 : 0);
+  if (n == 64) {
+    if (key == 4) launch(mma_probe<0, 0, 64, 1>); else return 1;
+  } else if (n == 256) {
+    if (key == 4) launch(mma_probe<0, 0, 256, 1>); else if (key == 0) launch(mma_probe<0, 0, 256, 0>); else return 1;
+  } else {
+    switch (key) {
+      case 0: launch(mma_probe<0, 0, 128, 0>); break;
+      case 1: launch(mma_probe<1, 0, 128, 0>); break;
+      case 2: launch(mma_probe<0, 1, 128, 0>); break;
+      case 3: launch(mma_probe<1, 1, 128, 0>); break;
+      case 4: launch(mma_probe<0, 0, 128, 1>); break;
+      case 5: launch(mma_probe<1, 0, 128, 1>); break;
+      case 6: launch(mma_probe<0, 1, 128, 1>); break;
+      default: launch(mma_probe<1, 1, 128, 1>); break;
+    }
+  }
   return finish(d_out, d_status, nullptr, out_cycles, n_ctas);
 }
 

@@ -49,9 +49,9 @@ def _median(fn, *args, n_ctas):
 
 
 MMA_CASES = [  # (a_tmem, b_mn, n, issuers, uniform)
-    (0, 0, 128, 1, 0), (0, 0, 128, 1, 1), (0, 0, 256, 1, 1), (0, 0, 64, 1, 1),
+    (0, 0, 128, 1, 0), (0, 0, 128, 1, 1), (0, 0, 256, 1, 1), (0, 0, 256, 1, 0), (0, 0, 64, 1, 1),
     (0, 1, 128, 1, 1), (1, 0, 128, 1, 1), (1, 1, 128, 1, 1), (1, 1, 128, 1, 0),
-    (0, 0, 128, 2, 1), (1, 1, 128, 2, 1), (1, 1, 128, 3, 1),
+    (0, 0, 128, 2, 1), (1, 1, 128, 2, 1), (1, 1, 128, 2, 0), (1, 1, 128, 3, 1),
 ]
 
 

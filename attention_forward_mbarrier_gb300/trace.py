@@ -39,10 +39,12 @@ def load_trace_lib(flags=()):
                            + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p])
     L.fmha_debug_set_trace.restype = ctypes.c_int
     L.fmha_debug_set_trace.argtypes = [ctypes.c_void_p]
+    L.fmha_debug_set_cta_trace.restype = ctypes.c_int
+    L.fmha_debug_set_cta_trace.argtypes = [ctypes.c_void_p]
     return L
 
 
-def run(w: wl.Workload, repeats: int = 3, flags=()):
+def run(w: wl.Workload, repeats: int = 3, flags=(), flush_l2: bool = True):
     """Stamps of the last of `repeats` launches: [query blocks, SLOTS] int64."""
     L = load_trace_lib(flags)
     dev = torch.device("cuda:0")
@@ -54,25 +56,46 @@ def run(w: wl.Workload, repeats: int = 3, flags=()):
     lse = torch.empty((w.heads, w.total_q), dtype=torch.float32, device=dev)
     pairs = (w.max_seqlen_q + 255) // 256
     buf = torch.zeros((pairs, SLOTS), dtype=torch.int64, device=dev)
+    ctas = torch.zeros((w.heads * pairs * w.batch, 4), dtype=torch.int64, device=dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream().cuda_stream
 
     def ptr(t):
         return None if t is None else t.data_ptr()
 
-    if L.fmha_debug_set_trace(buf.data_ptr()) != 0:
+    if L.fmha_debug_set_trace(buf.data_ptr()) != 0 or L.fmha_debug_set_cta_trace(ctas.data_ptr()) != 0:
         raise RuntimeError("fmha_debug_set_trace failed")
     try:
         for _ in range(repeats):
             buf.zero_()
+            ctas.zero_()
+            if flush_l2:
+                flush.zero_()  # the benchmark's L2 flush precedes every launch
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
             st = L.fmha_fwd(ptr(q), ptr(k), ptr(v), ptr(out), ptr(lse), ptr(cq), ptr(ck), w.batch,
                             w.total_q, w.total_k, w.max_seqlen_q, w.max_seqlen_k, w.heads,
                             w.head_dim, w.softmax_scale, int(w.causal), stream)
+            e1.record()
             if st != 0:
                 raise RuntimeError(f"fmha_fwd returned {st}")
             torch.cuda.synchronize()
+            run.last_event_ns = int(e0.elapsed_time(e1) * 1e6)
     finally:
         L.fmha_debug_set_trace(None)
-    return buf.cpu().numpy()
+        L.fmha_debug_set_cta_trace(None)
+    return buf.cpu().numpy(), ctas.cpu().numpy()
+
+
+def summarize_ctas(ctas: np.ndarray) -> dict:
+    """Spread of CTA entry / set-up / exit times (ns, relative to the first entry)."""
+    live = ctas[ctas[:, 0] > 0]
+    t0 = live[:, 0].min()
+    ent, setup, ext = live[:, 0] - t0, live[:, 1] - t0, live[:, 2] - t0
+    q = lambda a: [int(np.percentile(a, x)) for x in (0, 50, 100)]  # noqa: E731
+    return {"ctas": int(len(live)), "sms": int(len(np.unique(live[:, 3]))),
+            "entry_ns_min_med_max": q(ent), "setup_done_ns_min_med_max": q(setup),
+            "exit_ns_min_med_max": q(ext), "lifetime_ns_min_med_max": q(ext - ent)}
 
 
 def summarize(row: np.ndarray) -> dict:
@@ -119,13 +142,16 @@ def main():
     ap.add_argument("--row", type=int, default=0, help="query block (256 rows) of head 0 to show")
     ap.add_argument("--raw", default=None, help="save the raw stamps (.npy)")
     ap.add_argument("--flags", default="", help="extra -D flags for the trace build (tuning variants)")
+    ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush before each launch")
     args = ap.parse_args()
     w = wl.CONFIGS[args.workload]
-    stamps = run(w, flags=args.flags.split())
+    stamps, ctas = run(w, flags=args.flags.split(), flush_l2=not args.no_flush)
     if args.raw:
         np.save(args.raw, stamps)
     print(json.dumps({"workload": w.name, "flags": args.flags,
-                      "cycles_per_kv_step_median": summarize(stamps[args.row])}, indent=1))
+                      "cycles_per_kv_step_median": summarize(stamps[args.row]),
+                      "cta_times": summarize_ctas(ctas),
+                      "kernel_event_ns": run.last_event_ns, "l2_flushed": not args.no_flush}, indent=1))
 
 
 if __name__ == "__main__":

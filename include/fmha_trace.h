@@ -21,6 +21,14 @@ extern "C" {
  */
 int fmha_debug_set_trace(void *device_buffer);
 
+/*
+ * fmha_debug_set_cta_trace -- device_buffer: caller-owned device memory of
+ * (grid size) x 4 uint64, or NULL.  Every CTA writes, at its linear block id,
+ * %globaltimer (ns) at entry, after the set-up sync and at exit, and its SM
+ * id.  Returns FMHA_OK or FMHA_ERR_CUDA.
+ */
+int fmha_debug_set_cta_trace(void *device_buffer);
+
 #ifdef __cplusplus
 }
 #endif
