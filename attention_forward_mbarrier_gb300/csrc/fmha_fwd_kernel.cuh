@@ -78,6 +78,15 @@ static_assert(kBarKVEmpty == kBarKVFull + kStages && kBarSFull == kBarKVEmpty + 
 constexpr int kIssuers = FMHA_ISSUERS;
 static_assert(kIssuers == 1 || kIssuers == 2, "MMA issuers");
 
+// bf16 packing of P: cvt.rn (round to nearest even, default) or integer
+// round-half-up (-DFMHA_P_PACK_ALU=1; measured slower: it adds issue slots to
+// an exp loop that is issue-bound rather than limited by the conversion)
+#if defined(FMHA_P_PACK_ALU) && FMHA_P_PACK_ALU
+#define FMHA_P_PACK ptx::pack_bf16x2_alu
+#else
+#define FMHA_P_PACK ptx::pack_bf16x2
+#endif
+
 // roles, for the timeout detail word
 constexpr int kRoleSoftmax = 1, kRoleCorrection = 2, kRoleLoad = 3, kRoleMma = 4, kRoleDrain = 5;
 
@@ -86,7 +95,7 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 // Register budgets per warpgroup after the split (sum x 128 threads = 64K).
 // Helper calls in these regions must be inlined: ptxas cannot place an ABI
 // call inside a setmaxnreg region.
-constexpr int kRegsSoftmax = 184, kRegsCorrection = 64, kRegsControl = 80;
+constexpr int kRegsSoftmax = 192, kRegsCorrection = 48, kRegsControl = 80;
 static_assert(2 * kRegsSoftmax + kRegsCorrection + kRegsControl == 512, "register split");
 
 struct alignas(64) FwdParams {
@@ -193,13 +202,24 @@ __device__ __forceinline__ uint32_t col_o(int t) { return 256u + 128u * t; }
 // S_t = Q_t K^T: M=128 queries, N=128 keys, K=128 head dims in 8 steps of 16.
 // Q and K tiles are K-major with 128-byte swizzle: two 16 KiB halves (head dims
 // 0..63 and 64..127), rows 128 bytes apart, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ void issue_qk(uint32_t tmem_d, uint32_t q_addr, uint32_t k_addr) {
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) { return ptx::smem_desc_sw128(saddr, 16, 1024); }
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr) {
+  return ptx::smem_desc_sw128(saddr, kHalfBytes, 1024);
+}
+// A descriptor's start address is its low 14 bits in 16-byte units; every
+// offset below stays inside the 256 KiB window, so offsets add without carry.
+constexpr uint64_t kSlotDescStep = kTileBytes >> 4;
+
+// Each MMA is one instruction with a base descriptor plus an immediate offset:
+// a single issuing thread then keeps the tensor core fed (M128 N128 K16 every
+// 64 cycles, measured).
+__device__ __forceinline__ void issue_qk(uint32_t tmem_d, uint64_t q_desc, uint64_t k_desc) {
   constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, kBlockN, false, false);
+  ptx::mma_ss_imm<false>(tmem_d, q_desc, k_desc, idesc);
 #pragma unroll
-  for (int k = 0; k < kHeadDim / 16; ++k) {
-    const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32u;
-    ptx::mma_ss(tmem_d, ptx::smem_desc_sw128(q_addr + off, 16, 1024),
-                ptx::smem_desc_sw128(k_addr + off, 16, 1024), idesc, k > 0 ? 1u : 0u);
+  for (int k = 1; k < kHeadDim / 16; ++k) {
+    const uint64_t off = ((k >> 2) * kHalfBytes + (k & 3) * 32u) >> 4;
+    ptx::mma_ss_imm<true>(tmem_d, q_desc + off, k_desc + off, idesc);
   }
 }
 
@@ -208,14 +228,15 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_d, uint32_t q_addr, uint3
 // same swizzled layout as K: head dims contiguous within a 128-byte row, the
 // second 64 head dims 16 KiB further (leading offset), 8-key groups 1024
 // bytes apart (stride offset), 16 keys = 2048 bytes per step.
-__device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint32_t v_addr,
-                                         bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint64_t v_desc, bool accumulate) {
   constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, kHeadDim, false, true);
+  if (accumulate)
+    ptx::mma_ts_imm<true>(tmem_d, tmem_p, v_desc, idesc);
+  else
+    ptx::mma_ts_imm<false>(tmem_d, tmem_p, v_desc, idesc);
 #pragma unroll
-  for (int k = 0; k < kBlockN / 16; ++k) {
-    ptx::mma_ts(tmem_d, tmem_p + 8u * k, ptx::smem_desc_sw128(v_addr + 2048u * k, kHalfBytes, 1024),
-                idesc, (accumulate || k > 0) ? 1u : 0u);
-  }
+  for (int k = 1; k < kBlockN / 16; ++k)
+    ptx::mma_ts_imm<true>(tmem_d, tmem_p + 8u * k, v_desc + ((2048u * k) >> 4), idesc);
 }
 
 // ---------------------------------------------------------------------------
@@ -405,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           const float p0 = ptx::ex2_approx(x.x);
           const float p1 = ptx::ex2_approx(x.y);
           acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
-          pk[i] = ptx::pack_bf16x2(p0, p1);
+          pk[i] = FMHA_P_PACK(p0, p1);
         }
         ptx::tmem_st32(t_s + 32u * half, pk);
       }
@@ -529,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           ok = wait_bar(ctx, kBarQFull + t, 0, kRoleMma) && wait_bar(ctx, kBarKVFull + 0, 0, kRoleMma);
           if (ok) {
             ptx::tc_fence_after();
-            issue_qk(tmem + col_s(t), q_addr, base + kOffKV);
+            issue_qk(tmem + col_s(t), desc_kmajor(q_addr), desc_kmajor(base + kOffKV));
             ptx::mma_commit(ctx.bar(kBarSFull + t));
             ptx::mma_commit(ctx.bar(kBarKVEmpty + 0));
             issued_any = true;
@@ -545,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           const bool tr = j < kTrMaxBlocks;
           if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 1 + 2 * t);
           ptx::tc_fence_after();
-          issue_pv(tmem + col_o(t), tmem + col_s(t), base + kOffKV + vslot * kTileBytes, j > 0);
+          issue_pv(tmem + col_o(t), tmem + col_s(t), desc_mnmajor(base + kOffKV) + kSlotDescStep * vslot, j > 0);
           ptx::mma_commit(ctx.bar(kBarKVEmpty + vslot));
           if (j + 1 < nb) {
             const int kidx = 2 * j + 2, kslot = kidx % kStages;
@@ -554,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
               break;
             }
             ptx::tc_fence_after();
-            issue_qk(tmem + col_s(t), q_addr, base + kOffKV + kslot * kTileBytes);
+            issue_qk(tmem + col_s(t), desc_kmajor(q_addr), desc_kmajor(base + kOffKV) + kSlotDescStep * kslot);
             ptx::mma_commit(ctx.bar(kBarSFull + t));
             ptx::mma_commit(ctx.bar(kBarKVEmpty + kslot));
           } else {
@@ -579,6 +600,9 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     } else if (kIssuers == 1 && warp == 13) {
       // =============================== MMA issuer
       if (lane == 0) {
+        const uint64_t q_desc[kTiles] = {desc_kmajor(base + kOffQ), desc_kmajor(base + kOffQ + kTileBytes)};
+        const uint64_t kv_desc = desc_kmajor(base + kOffKV);
+        const uint64_t kv_desc_mn = desc_mnmajor(base + kOffKV);
         bool issued_any = false;
         bool ok = true;
 #pragma unroll
@@ -591,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
 #pragma unroll
           for (int t = 0; t < kTiles; ++t) {
             if (n_blk(t) > 0) {
-              issue_qk(tmem + col_s(t), base + kOffQ + t * kTileBytes, k_addr);
+              issue_qk(tmem + col_s(t), q_desc[t], kv_desc);
               ptx::mma_commit(ctx.bar(kBarSFull + t));
             }
           }
@@ -614,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
               }
               if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 1 + 2 * t);
               ptx::tc_fence_after();
-              issue_pv(tmem + col_o(t), tmem + col_s(t), base + kOffKV + vslot * kTileBytes, j > 0);
+              issue_pv(tmem + col_o(t), tmem + col_s(t), desc_mnmajor(base + kOffKV) + kSlotDescStep * vslot, j > 0);
               if (j + 1 < n_blk(t)) {
                 if (!k_ready) {
                   if (!wait_bar(ctx, kBarKVFull + kslot, (kidx / kStages) & 1, kRoleMma)) {
@@ -624,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
                   ptx::tc_fence_after();
                   k_ready = true;
                 }
-                issue_qk(tmem + col_s(t), base + kOffQ + t * kTileBytes, base + kOffKV + kslot * kTileBytes);
+                issue_qk(tmem + col_s(t), q_desc[t], kv_desc + kSlotDescStep * kslot);
                 ptx::mma_commit(ctx.bar(kBarSFull + t));
               } else {
                 ptx::mma_commit(ctx.bar(kBarOFinal + t));

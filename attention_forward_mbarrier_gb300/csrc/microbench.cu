@@ -5,7 +5,8 @@
 // hoisted, %clock64 around the timed loop with a memory clobber.
 //
 // fmha_microbench_alu(which): 0 ex2.approx.ftz.f32, 1 cvt.rn.bf16x2.f32,
-//   2 fma.rn.f32x2.  512 threads per SM.
+//   2 fma.rn.f32x2 (512 threads per SM); 3 the softmax exp loop of one
+//   128-score row per thread, 4 ex2 alone (128 threads per SM).
 // fmha_microbench_mma(...): back-to-back tcgen05.mma kind::f16 M=128 from
 //   `issuers` warps, each rotating nothing (one accumulator per issuer):
 //   a_tmem   0 = A from shared memory (SS), 1 = A from tensor memory (TS)
@@ -69,6 +70,52 @@ __global__ void __launch_bounds__(kAluThreads, 1) alu_probe(int which, int reps,
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc += v[i] + w[i].x + w[i].y;
   sink[blockIdx.x * kAluThreads + threadIdx.x] = acc;
+  if (threadIdx.x == 0) out[blockIdx.x] = t1 - t0;
+}
+
+// The attention softmax's exp loop in isolation, 128 threads (one warp per SM
+// sub-partition, as in the kernel): per row 128 scores -> one packed FMA per
+// pair, two ex2, packed row-sum add, bf16x2 pack; the packed P goes to shared
+// memory so nothing is dead code.  which 3: as is; which 4: ex2 only at one
+// warp per sub-partition (8 chains).
+__global__ void __launch_bounds__(128, 1) softmax_exp_probe(int which, int reps, long long* out, float* sink) {
+  __shared__ uint32_t sp[128 * 65];
+  float s[128];
+#pragma unroll
+  for (int k = 0; k < 128; ++k) s[k] = 0.01f * ((threadIdx.x * 7 + k * 13) & 255) - 1.f;
+  const float c = 0.1275f, neg_mc = -1.5f;
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = 0.001f * (threadIdx.x + i);
+  __syncthreads();
+  long long t0, t1;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0)::"memory");
+  if (which == 3) {
+    const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_mc, neg_mc);
+    for (int r = 0; r < reps; ++r) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), c2, nm2);
+        const float p0 = ptx::ex2_approx(x.x);
+        const float p1 = ptx::ex2_approx(x.y);
+        acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
+        sp[threadIdx.x * 65 + i] = ptx::pack_bf16x2(p0, p1);
+      }
+      s[r & 127] += 1e-7f;  // the next repetition depends on this one
+    }
+  } else {
+    for (int r = 0; r < reps; ++r) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = ptx::ex2_approx(v[i]) * -0.5f;
+    }
+  }
+  __syncthreads();
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1)::"memory");
+  float a = acc[0].x + acc[1].y + acc[2].x + acc[3].y + static_cast<float>(sp[threadIdx.x * 65 + 3] & 1u);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a += v[i];
+  sink[blockIdx.x * 128 + threadIdx.x] = a;
   if (threadIdx.x == 0) out[blockIdx.x] = t1 - t0;
 }
 
@@ -209,17 +256,37 @@ bool alloc(long long** d_out, int** d_status, int n_ctas) {
   return cudaMemset(*d_status, 0, 2 * sizeof(int)) == cudaSuccess;
 }
 
+__global__ void smem_touch_kernel(int* sink) {
+  extern __shared__ int sm[];
+  if (threadIdx.x == 0 && sink == nullptr) sm[0] = 1;  // never true; keeps the allocation
+}
+
 }  // namespace
 
+// Launch an empty kernel that requests `smem_bytes` of dynamic shared memory
+// per CTA on n_ctas CTAs (no synchronisation).  Used to see what a shared
+// memory carve-out change costs the next kernel.  Returns 0 or 2.
+extern "C" int fmha_microbench_smem_touch(int smem_bytes, int n_ctas, void* stream) {
+  if (cudaFuncSetAttribute(smem_touch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
+    return 2;
+  int one = 1;
+  int* dummy = reinterpret_cast<int*>(&one);
+  smem_touch_kernel<<<n_ctas, 128, smem_bytes, static_cast<cudaStream_t>(stream)>>>(dummy);
+  return cudaGetLastError() == cudaSuccess ? 0 : 2;
+}
+
 extern "C" int fmha_microbench_alu(int which, int reps, long long* out_cycles, int n_ctas) {
-  if (which < 0 || which > 2 || reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
+  if (which < 0 || which > 4 || reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
   long long* d_out = nullptr;
   int* d_status = nullptr;
   float* d_sink = nullptr;
   if (!alloc(&d_out, &d_status, n_ctas) ||
       cudaMalloc(&d_sink, sizeof(float) * n_ctas * kAluThreads) != cudaSuccess)
     return 2;
-  alu_probe<<<n_ctas, kAluThreads>>>(which, reps, d_out, d_sink);
+  if (which <= 2)
+    alu_probe<<<n_ctas, kAluThreads>>>(which, reps, d_out, d_sink);
+  else
+    softmax_exp_probe<<<n_ctas, 128>>>(which, reps, d_out, d_sink);
   return finish(d_out, d_status, d_sink, out_cycles, n_ctas);
 }
 

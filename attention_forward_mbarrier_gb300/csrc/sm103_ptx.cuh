@@ -160,6 +160,30 @@ __device__ __forceinline__ void mma_commit_leader(uint32_t bar, uint32_t leader)
       : "memory");
 }
 
+// Same MMAs with a compile-time accumulate flag (no predicate set-up per MMA).
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_ss_imm(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  if (kAccumulate)
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem), "l"(a_desc),
+                 "l"(b_desc), "r"(idesc)
+                 : "memory");
+  else
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d_tmem), "l"(a_desc),
+                 "l"(b_desc), "r"(idesc)
+                 : "memory");
+}
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_ts_imm(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
+  if (kAccumulate)
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem), "r"(a_tmem),
+                 "l"(b_desc), "r"(idesc)
+                 : "memory");
+  else
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 0;" ::"r"(d_tmem), "r"(a_tmem),
+                 "l"(b_desc), "r"(idesc)
+                 : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 async op issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -275,6 +299,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+
+// Pack two non-negative finite floats to bf16x2 with integer ops only (lo in
+// bits 0..15): add half a bf16 ulp to each bit pattern and keep the high
+// halves.  This rounds half up, which differs from round-to-nearest-even only
+// when the low 16 bits are exactly 0x8000, and keeps the conversion off the
+// unit that executes ex2.
+__device__ __forceinline__ uint32_t pack_bf16x2_alu(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo) + 0x8000u, __float_as_uint(hi) + 0x8000u, 0x7632);
 }
 
 // Pack two floats to bf16x2 (round to nearest even): lo in bits 0..15.

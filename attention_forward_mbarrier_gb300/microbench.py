@@ -66,6 +66,12 @@ def main():
         _median(L.fmha_microbench_alu, which, 64, n_ctas=sms)
         cyc = _median(L.fmha_microbench_alu, which, reps, n_ctas=sms)
         out[name + "_per_clk_per_sm"] = reps * 8 * 512 / cyc
+    _median(L.fmha_microbench_alu, 4, 64, n_ctas=sms)
+    cyc = _median(L.fmha_microbench_alu, 4, reps, n_ctas=sms)
+    out["ex2_per_clk_per_sm_one_warp_per_subpartition"] = reps * 8 * 128 / cyc
+    _median(L.fmha_microbench_alu, 3, 8, n_ctas=sms)
+    cyc = _median(L.fmha_microbench_alu, 3, 256, n_ctas=sms)
+    out["softmax_exp_loop_cycles_per_128_scores"] = cyc / 256
     mreps = 512
     rows = []
     for a_tmem, b_mn, n, issuers, uniform in MMA_CASES:
