@@ -51,7 +51,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kTiles * kTileBytes;
 constexpr uint32_t kOffBar = kOffKV + kStages * kTileBytes;
-constexpr uint32_t kNumBars = 21;
+constexpr uint32_t kNumBars = 22;
 constexpr uint32_t kOffMisc = kOffBar + 256;   // tmem base slot, abort flag
 constexpr uint32_t kOffAlpha = kOffBar + 512;  // float [2][128]
 constexpr uint32_t kSmemUsed = kOffAlpha + 1024;
@@ -67,6 +67,7 @@ constexpr int kBarPVReady = 12;   // [2]  P stored and O corrected for tile t
 constexpr int kBarAlpha = 14;     // [2]  softmax published this block's alpha
 constexpr int kBarOFinal = 16;    // [2]  last PV of tile t complete
 constexpr int kBarMmaDone = 18;   // [kIssuers] every MMA of an issuer retired
+constexpr int kBarPVReady2 = 20;  // [2]  second half of P stored (split hand-off)
 static_assert(kBarKVEmpty == kBarKVFull + kStages && kBarSFull == kBarKVEmpty + kStages, "ids");
 
 // MMA issuing warps: 1 = warp 13 issues both tiles in order; 2 = warp 13
@@ -86,6 +87,17 @@ static_assert(kIssuers == 1 || kIssuers == 2, "MMA issuers");
 #else
 #define FMHA_P_PACK ptx::pack_bf16x2
 #endif
+
+// P hand-off split ("Kernel Bottleneck Tuning", section "5. Tune the
+// producer->consumer handoff split"): with FMHA_P_SPLIT=1 the softmax signals
+// the PV issuer after the first 64 keys of P are in TMEM (P-ready-1, which also
+// carries the correction warps' arrivals) and again after the rest
+// (P-ready-2); the issuer issues exactly the first four PV k-steps (64 keys)
+// after the first signal, so it never reads a part of P not yet signalled.
+#ifndef FMHA_P_SPLIT
+#define FMHA_P_SPLIT 0
+#endif
+constexpr bool kPSplit = FMHA_P_SPLIT != 0;
 
 // roles, for the timeout detail word
 constexpr int kRoleSoftmax = 1, kRoleCorrection = 2, kRoleLoad = 3, kRoleMma = 4, kRoleDrain = 5;
@@ -228,15 +240,33 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_d, uint64_t q_desc, uint6
 // same swizzled layout as K: head dims contiguous within a 128-byte row, the
 // second 64 head dims 16 KiB further (leading offset), 8-key groups 1024
 // bytes apart (stride offset), 16 keys = 2048 bytes per step.
+template <int kBegin = 0, int kEnd = kBlockN / 16>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint64_t v_desc, bool accumulate) {
   constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, kHeadDim, false, true);
-  if (accumulate)
-    ptx::mma_ts_imm<true>(tmem_d, tmem_p, v_desc, idesc);
-  else
-    ptx::mma_ts_imm<false>(tmem_d, tmem_p, v_desc, idesc);
+  if (kBegin == 0) {
+    if (accumulate)
+      ptx::mma_ts_imm<true>(tmem_d, tmem_p, v_desc, idesc);
+    else
+      ptx::mma_ts_imm<false>(tmem_d, tmem_p, v_desc, idesc);
+  }
 #pragma unroll
-  for (int k = 1; k < kBlockN / 16; ++k)
+  for (int k = (kBegin == 0 ? 1 : kBegin); k < kEnd; ++k)
     ptx::mma_ts_imm<true>(tmem_d, tmem_p + 8u * k, v_desc + ((2048u * k) >> 4), idesc);
+}
+
+// PV of one tile: whole, or (split hand-off) the first 64 keys, a wait for the
+// second half of P, then the rest.  False if that wait gave up.
+__device__ __forceinline__ bool issue_pv_handoff(const Ctx& c, int t, int j, uint32_t tmem_d, uint32_t tmem_p,
+                                                 uint64_t v_desc, bool accumulate) {
+  if (!kPSplit) {
+    issue_pv(tmem_d, tmem_p, v_desc, accumulate);
+    return true;
+  }
+  issue_pv<0, 4>(tmem_d, tmem_p, v_desc, accumulate);
+  if (!wait_bar(c, kBarPVReady2 + t, j & 1, kRoleMma)) return false;
+  ptx::tc_fence_after();
+  issue_pv<4, 8>(tmem_d, tmem_p, v_desc, true);
+  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -328,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       ptx::mbar_init(ctx.bar(kBarSFull + t), 1);
       ptx::mbar_init(ctx.bar(kBarPVReady + t), 8);  // 4 softmax warps + 4 correction warps
       ptx::mbar_init(ctx.bar(kBarAlpha + t), 4);    // 4 softmax warps
+      ptx::mbar_init(ctx.bar(kBarPVReady2 + t), 4);  // 4 softmax warps
       ptx::mbar_init(ctx.bar(kBarOFinal + t), 1);
     }
     for (int s = 0; s < kStages; ++s) {
@@ -429,6 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           pk[i] = FMHA_P_PACK(p0, p1);
         }
         ptx::tmem_st32(t_s + 32u * half, pk);
+        if (kPSplit && half == 0) {  // first 64 keys of P to the PV issuer
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVReady + t));
+        }
       }
       const float2 a01 = __fadd2_rn(acc[0], acc[1]);
       const float2 a23 = __fadd2_rn(acc[2], acc[3]);
@@ -438,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVReady + t));
+      if (lane == 0) ptx::mbar_arrive(ctx.bar(kPSplit ? kBarPVReady2 + t : kBarPVReady + t));
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 4);
     }
     // ---- epilogue of this tile: LSE and O / l -> bf16 (rows of the sequence only),
@@ -566,7 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           const bool tr = j < kTrMaxBlocks;
           if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 1 + 2 * t);
           ptx::tc_fence_after();
-          issue_pv(tmem + col_o(t), tmem + col_s(t), desc_mnmajor(base + kOffKV) + kSlotDescStep * vslot, j > 0);
+          if (!issue_pv_handoff(ctx, t, j, tmem + col_o(t), tmem + col_s(t),
+                                desc_mnmajor(base + kOffKV) + kSlotDescStep * vslot, j > 0)) {
+            ok = false;
+            break;
+          }
           ptx::mma_commit(ctx.bar(kBarKVEmpty + vslot));
           if (j + 1 < nb) {
             const int kidx = 2 * j + 2, kslot = kidx % kStages;
@@ -638,7 +679,11 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
               }
               if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 1 + 2 * t);
               ptx::tc_fence_after();
-              issue_pv(tmem + col_o(t), tmem + col_s(t), desc_mnmajor(base + kOffKV) + kSlotDescStep * vslot, j > 0);
+              if (!issue_pv_handoff(ctx, t, j, tmem + col_o(t), tmem + col_s(t),
+                                    desc_mnmajor(base + kOffKV) + kSlotDescStep * vslot, j > 0)) {
+                ok = false;
+                break;
+              }
               if (j + 1 < n_blk(t)) {
                 if (!k_ready) {
                   if (!wait_bar(ctx, kBarKVFull + kslot, (kidx / kStages) & 1, kRoleMma)) {
