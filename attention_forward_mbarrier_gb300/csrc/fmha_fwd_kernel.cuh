@@ -14,13 +14,15 @@
 //   warpgroup 0, 1  softmax for tile 0 / tile 1: tcgen05.ld the S row, track
 //                   the running max, fold scale and -max into one packed FMA,
 //                   ex2, row sum, convert P to bf16 and tcgen05.st it over S;
+//                   then the tile's epilogue (O / l -> bf16 global, LSE);
 //   warpgroup 2     correction: rescales the O accumulator in TMEM when a row
-//                   max moved, and the epilogue (O / l -> bf16 global);
+//                   max moved;
 //   warp 12         TMA producer: Q tiles once, then a K/V ring in shared
-//                   memory gated by full/empty mbarriers;
+//                   memory whose slots the MMA warp's step commits free;
 //   warp 13         MMA issuer: tcgen05.mma S = Q K^T (both operands in
 //                   shared memory) and O += P V (P from TMEM), completion
-//                   signalled with tcgen05.commit on mbarriers.
+//                   signalled with tcgen05.commit on mbarriers;
+//   warps 14, 15    idle (barrier observers in the trace build).
 // Tensor memory (512 columns): S0/P0 [0,128), S1/P1 [128,256), O0 [256,384),
 // O1 [384,512).  P (bf16 pairs) overwrites the first 64 columns of its S.
 //
@@ -41,7 +43,9 @@ constexpr int kHeadDim = 128;
 constexpr int kBlockM = 128;   // query rows per tile (MMA M)
 constexpr int kBlockN = 128;   // keys per block (MMA N of QK^T, K of PV)
 constexpr int kTiles = 2;      // query tiles per CTA
-constexpr int kStages = 4;     // K/V ring slots (each holds one K or one V block)
+// K/V ring: four slots, each holding one K or one V block (two key blocks in
+// flight).  The slot-release protocol below relies on exactly four.
+constexpr int kStages = 4;
 constexpr int kThreads = 512;
 constexpr uint32_t kTileBytes = kBlockM * kHeadDim * 2;  // 32 KiB bf16 tile
 constexpr uint32_t kHalfBytes = kTileBytes / 2;          // 64 columns x 128 rows
@@ -51,58 +55,61 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kTiles * kTileBytes;
 constexpr uint32_t kOffBar = kOffKV + kStages * kTileBytes;
-constexpr uint32_t kNumBars = 22;
+constexpr uint32_t kNumBars = 16;
 constexpr uint32_t kOffMisc = kOffBar + 256;   // tmem base slot, abort flag
 constexpr uint32_t kOffAlpha = kOffBar + 512;  // float [2][128]
 constexpr uint32_t kSmemUsed = kOffAlpha + 1024;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kNumBars * 8 <= 256, "barrier area");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
-// barrier ids
-constexpr int kBarQFull = 0;      // [2]
-constexpr int kBarKVFull = 2;     // [kStages]
-constexpr int kBarKVEmpty = 6;    // [kStages]
-constexpr int kBarSFull = 10;     // [2]  QK^T of tile t landed in TMEM
-constexpr int kBarPVReady = 12;   // [2]  P stored and O corrected for tile t
-constexpr int kBarAlpha = 14;     // [2]  softmax published this block's alpha
-constexpr int kBarOFinal = 16;    // [2]  last PV of tile t complete
-constexpr int kBarMmaDone = 18;   // [kIssuers] every MMA of an issuer retired
-constexpr int kBarPVReady2 = 20;  // [2]  second half of P stored (split hand-off)
-static_assert(kBarKVEmpty == kBarKVFull + kStages && kBarSFull == kBarKVEmpty + kStages, "ids");
-
-// MMA issuing warps: 1 = warp 13 issues both tiles in order; 2 = warp 13
-// issues tile 0 and warp 14 tile 1, so a tile's P hand-off never waits behind
-// the other tile's MMA issue.
-#ifndef FMHA_ISSUERS
-#define FMHA_ISSUERS 1
-#endif
-constexpr int kIssuers = FMHA_ISSUERS;
-static_assert(kIssuers == 1 || kIssuers == 2, "MMA issuers");
+// Barrier ids.  Every tcgen05.commit stalls the tensor pipe for ~70-140
+// cycles (measured), so the MMA warp commits twice per KV step: S ready for
+// tile 0 when both tiles run, and one step commit.  Step commit n (n = 0 after
+// the first QK^T, n = j + 1 after step j) goes to StepDone[n & 1]; it tells the
+// last tile of the step that its S is ready and the producer that the step's
+// ring slots are free.
+constexpr int kBarQFull = 0;     // [2]
+constexpr int kBarKVFull = 2;    // [kStages]
+constexpr int kBarStepDone = 6;  // [2]  step commit n, alternating
+constexpr int kBarSFull0 = 8;    //      QK^T of tile 0 landed (tile 0 not the last tile)
+constexpr int kBarPVReady = 9;   // [2]  P stored and O corrected for tile t
+constexpr int kBarAlpha = 11;    // [2]  softmax published this block's alpha
+constexpr int kBarOFinal = 13;   // [2]  last PV of tile t complete
+constexpr int kBarMmaDone = 15;  //      every MMA retired
+static_assert(kBarMmaDone + 1 == static_cast<int>(kNumBars), "ids");
 
 // bf16 packing of P: cvt.rn (round to nearest even, default) or integer
-// round-half-up (-DFMHA_P_PACK_ALU=1; measured slower: it adds issue slots to
-// an exp loop that is issue-bound rather than limited by the conversion)
+// round-half-up (-DFMHA_P_PACK_ALU=1)
 #if defined(FMHA_P_PACK_ALU) && FMHA_P_PACK_ALU
 #define FMHA_P_PACK ptx::pack_bf16x2_alu
 #else
 #define FMHA_P_PACK ptx::pack_bf16x2
 #endif
 
-// P hand-off split ("Kernel Bottleneck Tuning", section "5. Tune the
-// producer->consumer handoff split"): with FMHA_P_SPLIT=1 the softmax signals
-// the PV issuer after the first 64 keys of P are in TMEM (P-ready-1, which also
-// carries the correction warps' arrivals) and again after the rest
-// (P-ready-2); the issuer issues exactly the first four PV k-steps (64 keys)
-// after the first signal, so it never reads a part of P not yet signalled.
-#ifndef FMHA_P_SPLIT
-#define FMHA_P_SPLIT 0
+// Warpgroup of each role.  Warp w reaches TMEM lanes 32 (w % 4) .. + 31, so
+// any warpgroup can hold a tile's softmax.  FMHA_CONTROL_FIRST=1 puts the
+// producer / MMA warpgroup at warps 0-3 instead of 12-15.
+#ifndef FMHA_CONTROL_FIRST
+#define FMHA_CONTROL_FIRST 0
 #endif
-constexpr bool kPSplit = FMHA_P_SPLIT != 0;
+constexpr int kWgControl = FMHA_CONTROL_FIRST ? 0 : 3;
+constexpr int kWgSoftmax0 = FMHA_CONTROL_FIRST ? 1 : 0;  // softmax of tile 0; tile 1 is the next warpgroup
+constexpr int kWgCorrection = FMHA_CONTROL_FIRST ? 3 : 2;
+constexpr int kWarpProducer = 4 * kWgControl;      // TMA producer, barrier set-up
+constexpr int kWarpMma = 4 * kWgControl + 1;       // MMA issuer, TMEM owner
 
 // roles, for the timeout detail word
 constexpr int kRoleSoftmax = 1, kRoleCorrection = 2, kRoleLoad = 3, kRoleMma = 4, kRoleDrain = 5;
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
+#ifndef FMHA_WAIT_HINT_NS
+#define FMHA_WAIT_HINT_NS 0
+#endif
+// A waiting thread sleeps inside mbarrier.try_wait for up to this long (it is
+// woken when the phase completes): polling warps would otherwise take issue
+// slots from the softmax warps on the same sub-partition.  0 = plain polling.
+constexpr uint32_t kWaitHintNs = FMHA_WAIT_HINT_NS;
 
 // Register budgets per warpgroup after the split (sum x 128 threads = 64K).
 // Helper calls in these regions must be inlined: ptxas cannot place an ABI
@@ -136,6 +143,11 @@ constexpr int kTrMma = 1040;        // + j * 8 + event
 constexpr int kTrCorrection = 1300; // + j * 8 + t * 4 + event
 constexpr int kTrLoad = 1600;       // + ring index
 constexpr int kTrMaxBlocks = 32;
+constexpr int kTrObsLoad = 272;  // + ring index (< 256): ring load landed
+constexpr int kTrObsStep = 784;  // + step commit n (< 128): its MMAs completed
+constexpr int kTrEpilogue = 1560;  // + 4 t + {0 O final seen, 1 O stored, 2 O staged}; 1568 after the final sync
+// set-up stamps: 2 entry, 3 barriers initialised, 4 first copies issued,
+// 5 TMEM allocated, 6 before the set-up sync (0 = after it)
 #ifdef FMHA_TRACE
 __device__ unsigned long long* g_trace;
 // per-CTA table (every CTA, linear block id): %globaltimer at entry, after the
@@ -161,7 +173,8 @@ struct Ctx {
 __device__ __forceinline__ bool wait_slow(const Ctx& c, uint32_t bar, uint32_t parity, int code) {
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (kWaitHintNs ? ptx::mbar_try_wait_sleep(bar, parity, kWaitHintNs) : ptx::mbar_try_wait(bar, parity))
+      return true;
     if (*c.abort_flag) return false;
     if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
       *c.abort_flag = 1u;
@@ -187,7 +200,7 @@ __device__ __forceinline__ bool wait_bar_warp(const Ctx& c, int id, uint32_t par
 __device__ __forceinline__ void wait_drain(const Ctx& c, int id, uint32_t parity) {
   const uint32_t b = c.bar(id);
   const uint64_t t0 = ptx::globaltimer_ns();
-  while (!ptx::mbar_try_wait(b, parity)) {
+  while (!(kWaitHintNs ? ptx::mbar_try_wait_sleep(b, parity, kWaitHintNs) : ptx::mbar_try_wait(b, parity))) {
     if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
       atomicCAS(&g_status, 0, 1 + kRoleDrain * 256 + id);
       return;
@@ -240,33 +253,15 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_d, uint64_t q_desc, uint6
 // same swizzled layout as K: head dims contiguous within a 128-byte row, the
 // second 64 head dims 16 KiB further (leading offset), 8-key groups 1024
 // bytes apart (stride offset), 16 keys = 2048 bytes per step.
-template <int kBegin = 0, int kEnd = kBlockN / 16>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint64_t v_desc, bool accumulate) {
   constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, kHeadDim, false, true);
-  if (kBegin == 0) {
-    if (accumulate)
-      ptx::mma_ts_imm<true>(tmem_d, tmem_p, v_desc, idesc);
-    else
-      ptx::mma_ts_imm<false>(tmem_d, tmem_p, v_desc, idesc);
-  }
+  if (accumulate)
+    ptx::mma_ts_imm<true>(tmem_d, tmem_p, v_desc, idesc);
+  else
+    ptx::mma_ts_imm<false>(tmem_d, tmem_p, v_desc, idesc);
 #pragma unroll
-  for (int k = (kBegin == 0 ? 1 : kBegin); k < kEnd; ++k)
+  for (int k = 1; k < kBlockN / 16; ++k)
     ptx::mma_ts_imm<true>(tmem_d, tmem_p + 8u * k, v_desc + ((2048u * k) >> 4), idesc);
-}
-
-// PV of one tile: whole, or (split hand-off) the first 64 keys, a wait for the
-// second half of P, then the rest.  False if that wait gave up.
-__device__ __forceinline__ bool issue_pv_handoff(const Ctx& c, int t, int j, uint32_t tmem_d, uint32_t tmem_p,
-                                                 uint64_t v_desc, bool accumulate) {
-  if (!kPSplit) {
-    issue_pv(tmem_d, tmem_p, v_desc, accumulate);
-    return true;
-  }
-  issue_pv<0, 4>(tmem_d, tmem_p, v_desc, accumulate);
-  if (!wait_bar(c, kBarPVReady2 + t, j & 1, kRoleMma)) return false;
-  ptx::tc_fence_after();
-  issue_pv<4, 8>(tmem_d, tmem_p, v_desc, true);
-  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -280,6 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
   const int lane = threadIdx.x & 31;
 #ifdef FMHA_TRACE
   const size_t cta_lin = blockIdx.x + static_cast<size_t>(gridDim.x) * (blockIdx.y + static_cast<size_t>(gridDim.y) * blockIdx.z);
+  unsigned long long* trace_row = (g_trace != nullptr && blockIdx.x == 0 && blockIdx.z == 0)
+                                      ? g_trace + static_cast<size_t>(blockIdx.y) * kTraceSlots
+                                      : nullptr;
+  if (threadIdx.x == 0) FMHA_TRACE_AT(2);
   if (threadIdx.x == 0 && g_trace_ctas != nullptr) {
     g_trace_ctas[cta_lin * 4 + 0] = ptx::globaltimer_ns();
     uint32_t smid;
@@ -314,6 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
   const int n_blk1 = tile_blocks(m0 + kBlockM, lq, lk, p.causal);
   const bool active1 = m0 + kBlockM < lq;  // tile 0 is active whenever the unit exists
   const int n_kv = max(n_blk0, n_blk1);
+  // The last tile of every KV step: tile 1 whenever it has blocks (it never has
+  // fewer than tile 0: causal rows further down see more keys), else tile 0.
+  const int t_last = n_blk1 > 0 ? 1 : 0;
   auto n_blk = [&](int t) { return t ? n_blk1 : n_blk0; };
   auto active = [&](int t) { return t ? active1 : true; };
 
@@ -326,17 +328,14 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
   // TMA producer steps (one thread): the Q tiles, and ring load idx = K (even) or
   // V (odd) of key block idx / 2 into slot idx % kStages.
   const int xh = h * kHeadDim;
-  auto load_q = [&](uint64_t pol) {
-#pragma unroll
-    for (int t = 0; t < kTiles; ++t) {
-      if (n_blk(t) > 0) {
-        const uint32_t bar = ctx.bar(kBarQFull + t);
-        ptx::mbar_arrive_expect_tx(bar, kTileBytes);
-        const uint32_t dst = base + kOffQ + t * kTileBytes;
-        const int y = q0 + m0 + kBlockM * t;
-        ptx::tma_load_2d(dst, &p.tmap_q, bar, xh, y, pol);
-        ptx::tma_load_2d(dst + kHalfBytes, &p.tmap_q, bar, xh + 64, y, pol);
-      }
+  auto load_q = [&](int t, uint64_t pol) {
+    if (n_blk(t) > 0) {
+      const uint32_t bar = ctx.bar(kBarQFull + t);
+      ptx::mbar_arrive_expect_tx(bar, kTileBytes);
+      const uint32_t dst = base + kOffQ + t * kTileBytes;
+      const int y = q0 + m0 + kBlockM * t;
+      ptx::tma_load_2d(dst, &p.tmap_q, bar, xh, y, pol);
+      ptx::tma_load_2d(dst + kHalfBytes, &p.tmap_q, bar, xh + 64, y, pol);
     }
   };
   auto load_kv = [&](int idx, uint64_t pol) {
@@ -352,51 +351,56 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
   // ring loads issued before the CTA-wide set-up sync (the ring starts empty)
   const int early_loads = min(kStages, 2 * n_kv);
 
-  if (warp == 12 && lane == 0) {
+  if (warp == kWarpProducer && lane == 0) {
     for (int t = 0; t < kTiles; ++t) {
       ptx::mbar_init(ctx.bar(kBarQFull + t), 1);
-      ptx::mbar_init(ctx.bar(kBarSFull + t), 1);
+      ptx::mbar_init(ctx.bar(kBarStepDone + t), 1);
       ptx::mbar_init(ctx.bar(kBarPVReady + t), 8);  // 4 softmax warps + 4 correction warps
       ptx::mbar_init(ctx.bar(kBarAlpha + t), 4);    // 4 softmax warps
-      ptx::mbar_init(ctx.bar(kBarPVReady2 + t), 4);  // 4 softmax warps
       ptx::mbar_init(ctx.bar(kBarOFinal + t), 1);
     }
-    for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(ctx.bar(kBarKVFull + s), 1);
-      ptx::mbar_init(ctx.bar(kBarKVEmpty + s), kIssuers);  // one release per issuing warp
-    }
-    for (int i = 0; i < kIssuers; ++i) ptx::mbar_init(ctx.bar(kBarMmaDone + i), 1);
+    for (int s = 0; s < kStages; ++s) ptx::mbar_init(ctx.bar(kBarKVFull + s), 1);
+    ptx::mbar_init(ctx.bar(kBarSFull0), 1);
+    ptx::mbar_init(ctx.bar(kBarMmaDone), 1);
     *ctx.abort_flag = 0u;
     ptx::fence_mbar_init();
+    FMHA_TRACE_AT(3);
     // start the first copies now: they overlap the TMEM allocation and the sync
     ptx::prefetch_tensormap(&p.tmap_q);
     ptx::prefetch_tensormap(&p.tmap_k);
     ptx::prefetch_tensormap(&p.tmap_v);
-    load_q(ptx::policy_evict_first());
+    // what the first S needs first (Q_0, K_0), then the rest: at launch every
+    // CTA loads at once and DRAM bandwidth orders the arrivals
+    const uint64_t pol_q = ptx::policy_evict_first();
     const uint64_t pol_kv = ptx::policy_evict_last();
-    for (int idx = 0; idx < early_loads; ++idx) load_kv(idx, pol_kv);
+    load_q(0, pol_q);
+    if (early_loads > 0) load_kv(0, pol_kv);
+    load_q(1, pol_q);
+    for (int idx = 1; idx < early_loads; ++idx) load_kv(idx, pol_kv);
+    FMHA_TRACE_AT(4);
   }
-  if (warp == 13) {
+  if (warp == kWarpMma) {
     ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
+    if (lane == 0) FMHA_TRACE_AT(5);
   }
+#ifdef FMHA_TRACE
+  if (threadIdx.x == 0) FMHA_TRACE_AT(6);
+#endif
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 #ifdef FMHA_TRACE
-  unsigned long long* trace_row = (g_trace != nullptr && blockIdx.x == 0 && blockIdx.z == 0)
-                                      ? g_trace + static_cast<size_t>(blockIdx.y) * kTraceSlots
-                                      : nullptr;
   if (threadIdx.x == 0) FMHA_TRACE_AT(0);
   if (threadIdx.x == 0 && g_trace_ctas != nullptr) g_trace_ctas[cta_lin * 4 + 1] = ptx::globaltimer_ns();
 #endif
 
   const int wg = warp >> 2;
-  if (wg < 2) {
+  if (wg == kWgSoftmax0 || wg == kWgSoftmax0 + 1) {
     // =============================== softmax (tile t = wg)
     ptx::setmaxnreg_inc<kRegsSoftmax>();
-    const int t = wg;
+    const int t = wg - kWgSoftmax0;
     const int r = (warp & 3) * 32 + lane;  // row within the tile == TMEM lane
     const uint32_t t_s = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16) + col_s(t);
     const int row = m0 + kBlockM * t + r;  // sequence-local query index
@@ -407,7 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     float m_used = -INFINITY;
     float l = 0.f;
     for (int j = 0; j < nb; ++j) {
-      if (!wait_bar_warp(ctx, kBarSFull + t, j & 1, kRoleSoftmax)) break;
+      // S_t(j): step commit j for the step's last tile, else tile 0's own commit
+      const bool s_ok = t == t_last ? wait_bar_warp(ctx, kBarStepDone + (j & 1), (j >> 1) & 1, kRoleSoftmax)
+                                    : wait_bar_warp(ctx, kBarSFull0, j & 1, kRoleSoftmax);
+      if (!s_ok) break;
       const bool tr = (r == 0 && j < kTrMaxBlocks);
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 0);
       ptx::tc_fence_after();
@@ -460,12 +467,6 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           pk[i] = FMHA_P_PACK(p0, p1);
         }
         ptx::tmem_st32(t_s + 32u * half, pk);
-        if (kPSplit && half == 0) {  // first 64 keys of P to the PV issuer
-          ptx::tmem_wait_st();
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVReady + t));
-        }
       }
       const float2 a01 = __fadd2_rn(acc[0], acc[1]);
       const float2 a23 = __fadd2_rn(acc[2], acc[3]);
@@ -475,8 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ctx.bar(kPSplit ? kBarPVReady2 + t : kBarPVReady + t));
+      if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVReady + t));
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 4);
+      // the other three warps of the warpgroup stamp their own hand-off (skew)
+      if (lane == 0 && (warp & 3) != 0 && j < kTrMaxBlocks) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 4 + (warp & 3));
     }
     // ---- epilogue of this tile: LSE and O / l -> bf16 (rows of the sequence only),
     // as soon as this tile's last PV completed
@@ -487,34 +490,78 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     }
     if (active(t) && (nb == 0 || wait_bar_warp(ctx, kBarOFinal + t, 0, kRoleSoftmax))) {
       if (nb > 0) ptx::tc_fence_after();
+      if (r == 0) FMHA_TRACE_AT(kTrEpilogue + 4 * t + 0);
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const uint32_t t_o = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16) + col_o(t);
-      __nv_bfloat16* dst =
-          p.out + (static_cast<size_t>(q0 + row) * p.heads + h) * static_cast<size_t>(kHeadDim);
+      // Whole warp inside the sequence: stage its 32 rows of O in this tile's Q
+      // buffer (free once the tile's last MMA completed) in the 128-byte
+      // swizzled layout (conflict-free both ways), then read back so that each
+      // 16-byte store instruction of the warp covers two complete 256-byte
+      // rows.  A warp with rows past the sequence end stores its valid rows
+      // directly, one row per thread.
+      const bool staged_out = nb > 0 && __all_sync(0xffffffffu, valid);
+      if (staged_out) {
+        const uint32_t tile_smem = base + kOffQ + static_cast<uint32_t>(t) * kTileBytes;
+        const uint32_t row_addr = tile_smem + static_cast<uint32_t>(r) * 128u;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float o[32];
-        if (nb > 0) {
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
           ptx::tmem_ld32_wait(t_o + 32u * cc, o);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0.f;
-        }
-        if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cc);
+          const uint32_t half_addr = row_addr + static_cast<uint32_t>(cc >> 1) * kHalfBytes;
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 w;
-            w.x = ptx::pack_bf16x2(o[8 * v4 + 0] * inv, o[8 * v4 + 1] * inv);
-            w.y = ptx::pack_bf16x2(o[8 * v4 + 2] * inv, o[8 * v4 + 3] * inv);
-            w.z = ptx::pack_bf16x2(o[8 * v4 + 4] * inv, o[8 * v4 + 5] * inv);
-            w.w = ptx::pack_bf16x2(o[8 * v4 + 6] * inv, o[8 * v4 + 7] * inv);
-            d4[v4] = w;
+            const uint32_t chunk = static_cast<uint32_t>((cc & 1) * 4 + v4);  // 16-byte chunk in the 128-byte row
+            ptx::st_shared_v4(half_addr + ((chunk ^ static_cast<uint32_t>(r & 7)) << 4),
+                              ptx::pack_bf16x2(o[8 * v4 + 0] * inv, o[8 * v4 + 1] * inv),
+                              ptx::pack_bf16x2(o[8 * v4 + 2] * inv, o[8 * v4 + 3] * inv),
+                              ptx::pack_bf16x2(o[8 * v4 + 4] * inv, o[8 * v4 + 5] * inv),
+                              ptx::pack_bf16x2(o[8 * v4 + 6] * inv, o[8 * v4 + 7] * inv));
+          }
+        }
+        if (r == 0) FMHA_TRACE_AT(kTrEpilogue + 4 * t + 2);
+        __syncwarp();
+        // lanes 0-15: row 2i of the warp, lanes 16-31: row 2i + 1; lane & 15
+        // picks the 16-byte chunk (8 head dims) of the 256-byte row
+        const int k16 = lane & 15;
+        const uint32_t hf = static_cast<uint32_t>(k16 >> 3), c = static_cast<uint32_t>(k16 & 7);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int rt = 32 * (warp & 3) + 2 * i + (lane >> 4);  // row within the tile
+          const uint4 v = ptx::ld_shared_v4(tile_smem + hf * kHalfBytes + static_cast<uint32_t>(rt) * 128u +
+                                            ((c ^ static_cast<uint32_t>(rt & 7)) << 4));
+          __nv_bfloat16* dst =
+              p.out + (static_cast<size_t>(q0 + m0 + kBlockM * t + rt) * p.heads + h) * kHeadDim + 64 * hf + 8 * c;
+          *reinterpret_cast<uint4*>(dst) = v;
+        }
+      } else {
+        __nv_bfloat16* dst =
+            p.out + (static_cast<size_t>(q0 + row) * p.heads + h) * static_cast<size_t>(kHeadDim);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          if (nb > 0) {
+            ptx::tmem_ld32_wait(t_o + 32u * cc, o);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0.f;
+          }
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cc);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = ptx::pack_bf16x2(o[8 * v4 + 0] * inv, o[8 * v4 + 1] * inv);
+              w.y = ptx::pack_bf16x2(o[8 * v4 + 2] * inv, o[8 * v4 + 3] * inv);
+              w.z = ptx::pack_bf16x2(o[8 * v4 + 4] * inv, o[8 * v4 + 5] * inv);
+              w.w = ptx::pack_bf16x2(o[8 * v4 + 6] * inv, o[8 * v4 + 7] * inv);
+              d4[v4] = w;
+            }
           }
         }
       }
+      if (r == 0) FMHA_TRACE_AT(kTrEpilogue + 4 * t + 1);
     }
-  } else if (wg == 2) {
+  } else if (wg == kWgCorrection) {
     // =============================== correction
     ptx::setmaxnreg_dec<kRegsCorrection>();
     const int r = (warp & 3) * 32 + lane;
@@ -555,15 +602,17 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     }
   } else {
     ptx::setmaxnreg_dec<kRegsControl>();
-    if (warp == 12) {
+    if (warp == kWarpProducer) {
       // =============================== TMA producer (continues after the early loads)
       if (lane == 0) {
         const uint64_t pol_kv = ptx::policy_evict_last();
         int issued = early_loads;
         for (int idx = early_loads; idx < 2 * n_kv; ++idx) {
-          const int slot = idx % kStages;
-          const uint32_t ph = (idx / kStages) & 1;
-          if (!wait_bar(ctx, kBarKVEmpty + slot, ph ^ 1u, kRoleLoad)) break;
+          // the slot's previous block (load idx - 4) was last read by the MMAs
+          // of step commit n: K_s by QK^T(s) (commit s), V_s by PV(s) (commit s + 1)
+          const int prev = idx - kStages;
+          const int n = (prev >> 1) + (prev & 1);
+          if (!wait_bar(ctx, kBarStepDone + (n & 1), (n >> 1) & 1, kRoleLoad)) break;
           if (idx < 400) FMHA_TRACE_AT(kTrLoad + idx);
           load_kv(idx, pol_kv);
           ++issued;
@@ -576,70 +625,12 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           if (n_blk(t) > 0) wait_drain(ctx, kBarQFull + t, 0);
       }
       __syncwarp();
-    } else if (kIssuers == 2 && (warp == 13 || warp == 14)) {
-      // =============================== MMA issuer of one tile (t = warp - 13)
-      const int t = warp - 13;
-      if (lane == 0) {
-        const int nb = n_blk(t);
-        const uint32_t q_addr = base + kOffQ + t * kTileBytes;
-        bool ok = true, issued_any = false;
-        if (nb > 0) {
-          ok = wait_bar(ctx, kBarQFull + t, 0, kRoleMma) && wait_bar(ctx, kBarKVFull + 0, 0, kRoleMma);
-          if (ok) {
-            ptx::tc_fence_after();
-            issue_qk(tmem + col_s(t), desc_kmajor(q_addr), desc_kmajor(base + kOffKV));
-            ptx::mma_commit(ctx.bar(kBarSFull + t));
-            ptx::mma_commit(ctx.bar(kBarKVEmpty + 0));
-            issued_any = true;
-          }
-        }
-        for (int j = 0; j < nb && ok; ++j) {
-          const int vidx = 2 * j + 1, vslot = vidx % kStages;
-          if (!wait_bar(ctx, kBarKVFull + vslot, (vidx / kStages) & 1, kRoleMma) ||
-              !wait_bar(ctx, kBarPVReady + t, j & 1, kRoleMma)) {
-            ok = false;
-            break;
-          }
-          const bool tr = j < kTrMaxBlocks;
-          if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 1 + 2 * t);
-          ptx::tc_fence_after();
-          if (!issue_pv_handoff(ctx, t, j, tmem + col_o(t), tmem + col_s(t),
-                                desc_mnmajor(base + kOffKV) + kSlotDescStep * vslot, j > 0)) {
-            ok = false;
-            break;
-          }
-          ptx::mma_commit(ctx.bar(kBarKVEmpty + vslot));
-          if (j + 1 < nb) {
-            const int kidx = 2 * j + 2, kslot = kidx % kStages;
-            if (!wait_bar(ctx, kBarKVFull + kslot, (kidx / kStages) & 1, kRoleMma)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            issue_qk(tmem + col_s(t), desc_kmajor(q_addr), desc_kmajor(base + kOffKV) + kSlotDescStep * kslot);
-            ptx::mma_commit(ctx.bar(kBarSFull + t));
-            ptx::mma_commit(ctx.bar(kBarKVEmpty + kslot));
-          } else {
-            ptx::mma_commit(ctx.bar(kBarOFinal + t));
-          }
-          if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 2 + 2 * t);
-        }
-        // K/V blocks loaded only for the other tile: release their slots
-        // unused, each after its copy landed (so the arrival counts toward
-        // that use of the slot)
-        for (int idx = 2 * nb; ok && idx < 2 * n_kv; ++idx) {
-          const int slot = idx % kStages;
-          if (!wait_bar(ctx, kBarKVFull + slot, (idx / kStages) & 1, kRoleMma)) break;
-          ptx::mbar_arrive(ctx.bar(kBarKVEmpty + slot));
-        }
-        if (issued_any) {  // all MMAs retired before TMEM is released
-          ptx::mma_commit(ctx.bar(kBarMmaDone + t));
-          wait_drain(ctx, kBarMmaDone + t, 0);
-        }
-      }
-      __syncwarp();
-    } else if (kIssuers == 1 && warp == 13) {
+    } else if (warp == kWarpMma) {
       // =============================== MMA issuer
+      // Per KV step j: for each tile with block j, PV_t(j) then QK^T_t(j + 1)
+      // (S_t and P_t share TMEM columns, so the next QK^T follows the PV), a
+      // commit for tile 0's S unless tile 0 is the step's last tile, and one
+      // step commit.
       if (lane == 0) {
         const uint64_t q_desc[kTiles] = {desc_kmajor(base + kOffQ), desc_kmajor(base + kOffQ + kTileBytes)};
         const uint64_t kv_desc = desc_kmajor(base + kOffKV);
@@ -652,15 +643,14 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         if (ok && n_kv > 0) ok = wait_bar(ctx, kBarKVFull + 0, 0, kRoleMma);
         if (ok && n_kv > 0) {
           ptx::tc_fence_after();
-          const uint32_t k_addr = base + kOffKV;
 #pragma unroll
           for (int t = 0; t < kTiles; ++t) {
             if (n_blk(t) > 0) {
               issue_qk(tmem + col_s(t), q_desc[t], kv_desc);
-              ptx::mma_commit(ctx.bar(kBarSFull + t));
+              if (t != t_last) ptx::mma_commit(ctx.bar(kBarSFull0));
             }
           }
-          ptx::mma_commit(ctx.bar(kBarKVEmpty + 0));
+          ptx::mma_commit(ctx.bar(kBarStepDone + 0));  // step commit 0
           issued_any = true;
           for (int j = 0; j < n_kv && ok; ++j) {
             const int vidx = 2 * j + 1, vslot = vidx % kStages;
@@ -679,11 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
               }
               if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 1 + 2 * t);
               ptx::tc_fence_after();
-              if (!issue_pv_handoff(ctx, t, j, tmem + col_o(t), tmem + col_s(t),
-                                    desc_mnmajor(base + kOffKV) + kSlotDescStep * vslot, j > 0)) {
-                ok = false;
-                break;
-              }
+              issue_pv(tmem + col_o(t), tmem + col_s(t), kv_desc_mn + kSlotDescStep * vslot, j > 0);
               if (j + 1 < n_blk(t)) {
                 if (!k_ready) {
                   if (!wait_bar(ctx, kBarKVFull + kslot, (kidx / kStages) & 1, kRoleMma)) {
@@ -693,16 +679,18 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
                   ptx::tc_fence_after();
                   k_ready = true;
                 }
+                if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 6 + t);
                 issue_qk(tmem + col_s(t), q_desc[t], kv_desc + kSlotDescStep * kslot);
-                ptx::mma_commit(ctx.bar(kBarSFull + t));
+                if (t != t_last) ptx::mma_commit(ctx.bar(kBarSFull0));
               } else {
                 ptx::mma_commit(ctx.bar(kBarOFinal + t));
               }
               if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 2 + 2 * t);
             }
             if (!ok) break;
-            ptx::mma_commit(ctx.bar(kBarKVEmpty + vslot));
-            if (k_ready) ptx::mma_commit(ctx.bar(kBarKVEmpty + kslot));
+            const int n = j + 1;  // step commit n: frees V_j's and K_(j+1)'s slots
+            ptx::mma_commit(ctx.bar(kBarStepDone + (n & 1)));
+            if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 5);
           }
         }
         if (issued_any) {  // all MMAs retired before TMEM is released
@@ -712,14 +700,39 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       }
       __syncwarp();
     }
+#ifdef FMHA_TRACE
+    else if (lane == 0 && trace_row != nullptr) {
+      // trace build only: warp 14 stamps when each ring load lands, warp 15
+      // when the MMAs of each step commit complete (short bounded polls that
+      // never raise the error word; a miss ends the observation)
+      auto observe = [&](int id, uint32_t parity) {
+        const uint64_t g0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(ctx.bar(id), parity))
+          if (ptx::globaltimer_ns() - g0 > 200000ull) return false;
+        return true;
+      };
+      if (warp == kWarpMma + 1) {
+        for (int idx = 0; idx < min(2 * n_kv, 256); ++idx) {
+          if (!observe(kBarKVFull + idx % kStages, (idx / kStages) & 1)) break;
+          FMHA_TRACE_AT(kTrObsLoad + idx);
+        }
+      } else {
+        for (int n = 0; n <= min(n_kv, 127); ++n) {
+          if (!observe(kBarStepDone + (n & 1), (n >> 1) & 1)) break;
+          FMHA_TRACE_AT(kTrObsStep + n);
+        }
+      }
+    }
+#endif
   }
 
 #ifdef FMHA_TRACE
-  if (warp == 8 && lane == 0) FMHA_TRACE_AT(1);
+  if (warp == 4 * kWgCorrection && lane == 0) FMHA_TRACE_AT(1);
 #endif
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 13) {
+  if (threadIdx.x == 0) FMHA_TRACE_AT(kTrEpilogue + 8);
+  if (warp == kWarpMma) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
 #ifdef FMHA_TRACE

@@ -29,6 +29,54 @@ namespace {
 
 using namespace fmha;
 
+// Probe-only arithmetic (the attention kernel does not use these).
+namespace ptx_probe {
+// 2^x of a pair on the FMA pipe instead of the MUFU: range reduction
+// 2^x = 2^n * 2^f with n = round(x), f = x - n in [-0.5, 0.5] (n taken from
+// the low mantissa bits of x + 1.5 * 2^23), and 2^f from a degree-3
+// polynomial whose coefficients were fitted here for minimal relative error
+// on [-0.5, 0.5] (Lawson-weighted least squares; max relative error 7.5e-5,
+// below half a bf16 ulp by a factor of 26).  x is clamped at -126, where 2^x
+// is below every normal fp32.
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  x.x = fmaxf(x.x, -126.f);
+  x.y = fmaxf(x.y, -126.f);
+  const float2 t = __fadd2_rn(x, make_float2(12582912.f, 12582912.f));
+  const float2 n = __fadd2_rn(t, make_float2(-12582912.f, -12582912.f));
+  const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), x);
+  float2 p = __ffma2_rn(make_float2(0.0551716648f, 0.0551716648f), f, make_float2(0.242611125f, 0.242611125f));
+  p = __ffma2_rn(p, f, make_float2(0.693260968f, 0.693260968f));
+  p = __ffma2_rn(p, f, make_float2(0.999928057f, 0.999928057f));
+  const uint32_t bx = __float_as_uint(p.x) + (__float_as_uint(t.x) << 23);
+  const uint32_t by = __float_as_uint(p.y) + (__float_as_uint(t.y) << 23);
+  return make_float2(__uint_as_float(bx), __uint_as_float(by));
+}
+
+// Two fp32 values -> packed f16x2 (round to nearest), lo in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// 2^x of both halves of a packed f16x2 (one MUFU instruction for two values).
+__device__ __forceinline__ uint32_t ex2_approx_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Packed f16x2 -> two fp32 (lo = low half).
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t h) {
+  float lo, hi;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
+  return make_float2(lo, hi);
+}
+
+}  // namespace ptx_probe
+
 constexpr int kAluThreads = 512;
 constexpr int kTcThreads = 128;
 // shared memory: zeroed A tile (32 KiB) and B tile (64 KiB), barriers
@@ -119,6 +167,83 @@ __global__ void __launch_bounds__(128, 1) softmax_exp_probe(int which, int reps,
   if (threadIdx.x == 0) out[blockIdx.x] = t1 - t0;
 }
 
+// Variants of the exp loop, `threads` = 128 (one warp per sub-partition, as
+// the kernel) or 256 (two): per repetition each thread turns 128 scores into
+// 64 packed pairs.  variant 0: packed FMA, two ex2, packed row-sum add,
+// cvt.rn bf16x2 pack; 1: without the pack; 2: ex2 + row sum only (no FMA, no
+// pack; hoisted by the compiler, not meaningful); 3: without the ex2 (FMA,
+// sum, pack); 4: as 0 with the integer pack; 5: the pair's exponent in f16x2
+// (one packed ex2 for two scores, then back to fp32 for the sum and the bf16
+// pack); 6: packed f16x2 ex2 alone, 8 chains, 64 per repetition; 7: as 0 with
+// one pair in four on the FMA pipe (exp2_poly2); 8: one pair in eight.
+// Packed words go to shared memory as 16-byte vectors; the offset the scores
+// are shifted by changes every repetition so nothing is hoisted.
+template <int variant, int threads>
+__global__ void __launch_bounds__(threads, 1) exp_loop_probe(int reps, long long* out, float* sink) {
+  __shared__ uint4 sp[threads * 8];
+  float s[128];
+#pragma unroll
+  for (int k = 0; k < 128; ++k) s[k] = 0.01f * ((threadIdx.x * 7 + k * 13) & 255) - 1.f;
+  const float c = 0.1275f;
+  float neg_mc = -1.5f;
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  uint32_t hv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) hv[i] = 0x3c00bc00u + threadIdx.x + i;  // (-1, 1) and nearby
+  __syncthreads();
+  long long t0, t1;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0)::"memory");
+  const float2 c2 = make_float2(c, c);
+  if (variant == 6) {
+    for (int r = 0; r < reps; ++r) {
+#pragma unroll
+      for (int rep8 = 0; rep8 < 8; ++rep8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hv[i] = ptx_probe::ex2_approx_f16x2(hv[i]) ^ 0x80008000u;
+      }
+    }
+  }
+  for (int r = 0; r < (variant == 6 ? 0 : reps); ++r) {
+    const float2 nm2 = make_float2(neg_mc, neg_mc);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int k = 8 * q + 2 * i;
+        float2 x = make_float2(s[k], s[k + 1]);
+        if (variant != 2) x = __ffma2_rn(x, c2, nm2);
+        float p0 = x.x, p1 = x.y;
+        if ((variant == 7 && i == 3) || (variant == 8 && i == 3 && (q & 1))) {
+          const float2 e = ptx_probe::exp2_poly2(x);
+          p0 = e.x;
+          p1 = e.y;
+        } else if (variant == 5) {
+          const float2 e = ptx_probe::unpack_f16x2(ptx_probe::ex2_approx_f16x2(ptx_probe::pack_f16x2(x.x, x.y)));
+          p0 = e.x;
+          p1 = e.y;
+        } else if (variant != 3) {
+          p0 = ptx::ex2_approx(x.x);
+          p1 = ptx::ex2_approx(x.y);
+        }
+        acc[i] = __fadd2_rn(acc[i], make_float2(p0, p1));
+        if (variant == 4)
+          pk[i] = ptx::pack_bf16x2_alu(p0, p1);
+        else
+          pk[i] = ptx::pack_bf16x2(p0, p1);
+      }
+      if (variant != 1 && variant != 2) sp[threadIdx.x * 8 + (q & 7)] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    neg_mc += 1e-7f;
+  }
+  __syncthreads();
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1)::"memory");
+  const uint4 w = sp[threadIdx.x * 8 + 3];
+  sink[blockIdx.x * threads + threadIdx.x] = acc[0].x + acc[1].y + acc[2].x + acc[3].y +
+                                             static_cast<float>((w.x ^ w.w ^ hv[0] ^ hv[5]) & 1u);
+  if (threadIdx.x == 0) out[blockIdx.x] = t1 - t0;
+}
+
 // Shared set-up of the tensor-core probes: zero the operand tiles, init one
 // barrier per warp, allocate all 512 TMEM columns.
 __device__ __forceinline__ uint32_t tc_setup(uint8_t* smem, uint32_t base) {
@@ -203,6 +328,150 @@ __global__ void __launch_bounds__(kTcThreads, 1) mma_probe(int issuers, int reps
       ptx::mma_commit(bar);
     if (!bounded_wait(bar)) status[0] = 1;
     asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1)::"memory");
+  }
+  __syncwarp();
+  tc_teardown(tmem);
+  if (threadIdx.x == 0) out[blockIdx.x] = t1 - t0;
+}
+
+// Issuing-thread cost of the step boundary: each round issues the 16 MMAs of
+// one tile group (8 PV + 8 QK^T), then mode 0: tcgen05.commit then
+// mbarrier.try_wait on an already-completed barrier; 1: the try_wait alone;
+// 2: the commit alone.  Returns the summed cycles of that boundary sequence.
+template <int mode>
+__global__ void __launch_bounds__(kTcThreads, 1) boundary_probe(int reps, long long* out, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t tmem = tc_setup(smem, base);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  long long acc = 0;
+  if (warp == 0 && lane == 0) {
+    const uint32_t done_bar = base + kMbBar + 24u;
+    ptx::mbar_arrive(done_bar);  // count 1: phase 0 completes now
+    const uint32_t id_qk = ptx::idesc_bf16_f32(128, 128, false, false);
+    const uint32_t id_pv = ptx::idesc_bf16_f32(128, 128, false, true);
+    const uint64_t q0 = ptx::smem_desc_sw128(base + kMbA, 16, 1024);
+    const uint64_t k0 = ptx::smem_desc_sw128(base + kMbB, 16, 1024);
+    const uint64_t v0 = ptx::smem_desc_sw128(base + kMbB + 32768u, 16384, 1024);
+    int fails = 0;
+    for (int r = 0; r < reps; ++r) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        ptx::mma_ts(tmem + 256u, tmem + 8u * k, v0 + ((2048u * k) >> 4), id_pv, 1u);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint64_t off = ((k >> 2) * 16384u + (k & 3) * 32u) >> 4;
+        ptx::mma_ss(tmem, q0 + off, k0 + off, id_qk, k > 0 ? 1u : 0u);
+      }
+      long long a, b;
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(a)::"memory");
+      if (mode != 1) ptx::mma_commit(base + kMbBar + 8u);
+      if (mode != 2 && !ptx::mbar_try_wait(done_bar, 0)) ++fails;
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(b)::"memory");
+      acc += b - a;
+    }
+    const uint32_t bar = base + kMbBar;
+    ptx::mma_commit(bar);
+    if (!bounded_wait(bar) || fails) status[0] = 1;
+  }
+  __syncwarp();
+  tc_teardown(tmem);
+  if (threadIdx.x == 0) out[blockIdx.x] = acc;
+}
+
+// The attention kernel's MMA stream without its waits: per tile t (0, 1) a
+// group of 8 PV MMAs (A = P from TMEM columns [128 t, 128 t + 64), B = V
+// MN-major) into O_t at columns 256 + 128 t, then 8 QK^T MMAs (A = Q, B = K,
+// both K-major in shared memory) into S_t at columns 128 t.  mode 0: that
+// stream; 1: only the QK^T MMAs; 2: only the PV MMAs; 3: the stream while
+// warps 1-3 write 16-byte vectors to a separate shared-memory buffer (TMA-like
+// write traffic) until the issuer is done; 4: tile 0's stream only while warps
+// 1-3 load TMEM columns [128, 256) and store columns [384, 512), which no MMA
+// of this mode touches (softmax-like TMEM traffic); 5: tile 0's stream alone;
+// 6: the two-tile stream with a tcgen05.commit after every 8 MMAs (as the
+// kernel signals S ready and frees ring slots); 7: a commit after every MMA;
+// 8: one commit per 32 MMAs; 9: tile 0's QK^T only, a commit after every 8.
+// In-loop commits go to a barrier nobody waits on.  P and S share columns
+// exactly as in the kernel (the next QK^T of a tile follows its PV).
+template <int mode>
+__global__ void __launch_bounds__(kTcThreads, 1) mma_mix_probe(int reps, long long* out, int* status) {
+  constexpr int n_tiles = (mode == 4 || mode == 5 || mode == 9) ? 1 : 2;
+  constexpr bool do_pv = mode != 1 && mode != 9;
+  constexpr bool do_qk = mode != 2;
+  constexpr bool commit_group = mode == 6 || mode == 9;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t tmem = tc_setup(smem, base);
+  volatile uint32_t* done_flag = reinterpret_cast<volatile uint32_t*>(smem + kMbBar + 96);
+  if (threadIdx.x == 0) *done_flag = 0u;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  long long t0 = 0, t1 = 0;
+  if (warp == 0) {
+    const uint32_t leader = lane == 0 ? 1u : 0u;
+    const uint32_t id_qk = ptx::idesc_bf16_f32(128, 128, false, false);
+    const uint32_t id_pv = ptx::idesc_bf16_f32(128, 128, false, true);
+    const uint64_t q0 = ptx::smem_desc_sw128(base + kMbA, 16, 1024);
+    const uint64_t k0 = ptx::smem_desc_sw128(base + kMbB, 16, 1024);
+    const uint64_t v0 = ptx::smem_desc_sw128(base + kMbB + 32768u, 16384, 1024);
+    const uint32_t spare = base + kMbBar + 8u;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0)::"memory");
+    for (int r = 0; r < reps; ++r) {
+#pragma unroll
+      for (int tl = 0; tl < n_tiles; ++tl) {
+        if (do_pv) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            ptx::mma_ts_leader(tmem + 256u + 128u * tl, tmem + 128u * tl + 8u * k, v0 + ((2048u * k) >> 4), id_pv,
+                               1u, leader);
+            if (mode == 7) ptx::mma_commit_leader(spare, leader);
+          }
+          if (commit_group) ptx::mma_commit_leader(spare, leader);
+        }
+        if (do_qk) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t off = ((k >> 2) * 16384u + (k & 3) * 32u) >> 4;
+            ptx::mma_ss_leader(tmem + 128u * tl, q0 + off, k0 + off, id_qk, k > 0 ? 1u : 0u, leader);
+            if (mode == 7) ptx::mma_commit_leader(spare, leader);
+          }
+          if (commit_group) ptx::mma_commit_leader(spare, leader);
+        }
+      }
+      if (mode == 8) ptx::mma_commit_leader(spare, leader);
+    }
+    const uint32_t bar = base + kMbBar;
+    ptx::mma_commit_leader(bar, leader);
+    if (!bounded_wait(bar)) status[0] = 1;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1)::"memory");
+    if (lane == 0) *done_flag = 1u;
+  } else if (mode == 4) {
+    const uint32_t lanes = (static_cast<uint32_t>(warp) * 32u) << 16;
+    float acc = 0.f;
+    for (int it = 0; it < (1 << 20) && *done_flag == 0u; ++it) {
+      float x[32];
+      ptx::tmem_ld32_wait(tmem + lanes + 128u + 32u * (it & 3), x);
+      uint32_t u[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(x[i] + 1.f);
+      ptx::tmem_st32(tmem + lanes + 384u + 32u * (it & 3), u);
+      ptx::tmem_wait_st();
+      acc += x[5];
+    }
+    if (acc == 12345.f) status[1] = 1;  // keeps the loads
+  } else if (mode == 3) {
+    // write traffic into [kMbBar + 128, + 32 KiB) (inside the launch's extra
+    // 32 KiB); bounded in iterations
+    uint4* dst = reinterpret_cast<uint4*>(smem + kMbBar + 128);
+    const uint4 val = make_uint4(threadIdx.x, 1u, 2u, 3u);
+    for (int it = 0; it < (1 << 22) && *done_flag == 0u; ++it) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[((it * 8 + i) * 96 + threadIdx.x - 32) & 2047] = val;
+    }
   }
   __syncwarp();
   tc_teardown(tmem);
@@ -321,6 +590,84 @@ extern "C" int fmha_microbench_mma(int a_tmem, int b_mn, int n, int issuers, int
     }
   }
   return finish(d_out, d_status, nullptr, out_cycles, n_ctas);
+}
+
+// Cycles of `reps` rounds of the attention MMA stream (32 MMAs a round) in
+// the given mode of mma_mix_probe.  Returns as fmha_microbench_mma.
+extern "C" int fmha_microbench_mma_mix(int mode, int reps, long long* out_cycles, int n_ctas) {
+  if (mode < 0 || mode > 9 || reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
+  long long* d_out = nullptr;
+  int* d_status = nullptr;
+  if (!alloc(&d_out, &d_status, n_ctas)) return 2;
+  const int smem = static_cast<int>(kMbSmem) + 32768;
+  auto launch = [&](auto kernel) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    kernel<<<n_ctas, kTcThreads, smem>>>(reps, d_out, d_status);
+  };
+  switch (mode) {
+    case 0: launch(mma_mix_probe<0>); break;
+    case 1: launch(mma_mix_probe<1>); break;
+    case 2: launch(mma_mix_probe<2>); break;
+    case 3: launch(mma_mix_probe<3>); break;
+    case 4: launch(mma_mix_probe<4>); break;
+    case 5: launch(mma_mix_probe<5>); break;
+    case 6: launch(mma_mix_probe<6>); break;
+    case 7: launch(mma_mix_probe<7>); break;
+    case 8: launch(mma_mix_probe<8>); break;
+    default: launch(mma_mix_probe<9>); break;
+  }
+  return finish(d_out, d_status, nullptr, out_cycles, n_ctas);
+}
+
+// Summed cycles of the step-boundary sequence of boundary_probe over `reps`
+// rounds.  Returns as fmha_microbench_mma.
+extern "C" int fmha_microbench_boundary(int mode, int reps, long long* out_cycles, int n_ctas) {
+  if (mode < 0 || mode > 2 || reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
+  long long* d_out = nullptr;
+  int* d_status = nullptr;
+  if (!alloc(&d_out, &d_status, n_ctas)) return 2;
+  auto launch = [&](auto kernel) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMbSmem));
+    kernel<<<n_ctas, kTcThreads, kMbSmem>>>(reps, d_out, d_status);
+  };
+  switch (mode) {
+    case 0: launch(boundary_probe<0>); break;
+    case 1: launch(boundary_probe<1>); break;
+    default: launch(boundary_probe<2>); break;
+  }
+  return finish(d_out, d_status, nullptr, out_cycles, n_ctas);
+}
+
+// Cycles for `reps` repetitions of exp_loop_probe<variant, threads>.
+extern "C" int fmha_microbench_exp_loop(int variant, int threads, int reps, long long* out_cycles, int n_ctas) {
+  if (variant < 0 || variant > 8 || (threads != 128 && threads != 256) || reps < 1 || n_ctas < 1 ||
+      out_cycles == nullptr)
+    return 1;
+  long long* d_out = nullptr;
+  int* d_status = nullptr;
+  float* d_sink = nullptr;
+  if (!alloc(&d_out, &d_status, n_ctas) || cudaMalloc(&d_sink, sizeof(float) * n_ctas * 256) != cudaSuccess)
+    return 2;
+#define FMHA_EXP_CASE(V)                                                   \
+  case V:                                                                  \
+    if (threads == 128)                                                    \
+      exp_loop_probe<V, 128><<<n_ctas, 128>>>(reps, d_out, d_sink);        \
+    else                                                                   \
+      exp_loop_probe<V, 256><<<n_ctas, 256>>>(reps, d_out, d_sink);        \
+    break;
+  switch (variant) {
+    FMHA_EXP_CASE(0)
+    FMHA_EXP_CASE(1)
+    FMHA_EXP_CASE(2)
+    FMHA_EXP_CASE(3)
+    FMHA_EXP_CASE(4)
+    FMHA_EXP_CASE(5)
+    FMHA_EXP_CASE(6)
+    FMHA_EXP_CASE(7)
+    FMHA_EXP_CASE(8)
+  }
+#undef FMHA_EXP_CASE
+  return finish(d_out, d_status, d_sink, out_cycles, n_ctas);
 }
 
 extern "C" int fmha_microbench_tmem_ld(int reps, long long* out_cycles, int n_ctas) {

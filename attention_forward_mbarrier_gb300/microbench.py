@@ -35,6 +35,12 @@ def load():
     L.fmha_microbench_alu.argtypes = [ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
     L.fmha_microbench_mma.restype = ctypes.c_int
     L.fmha_microbench_mma.argtypes = [ctypes.c_int] * 6 + [P, ctypes.c_int]
+    L.fmha_microbench_mma_mix.restype = ctypes.c_int
+    L.fmha_microbench_mma_mix.argtypes = [ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
+    L.fmha_microbench_boundary.restype = ctypes.c_int
+    L.fmha_microbench_boundary.argtypes = [ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
+    L.fmha_microbench_exp_loop.restype = ctypes.c_int
+    L.fmha_microbench_exp_loop.argtypes = [ctypes.c_int] * 3 + [P, ctypes.c_int]
     L.fmha_microbench_tmem_ld.restype = ctypes.c_int
     L.fmha_microbench_tmem_ld.argtypes = [ctypes.c_int, P, ctypes.c_int]
     return L
@@ -72,6 +78,17 @@ def main():
     _median(L.fmha_microbench_alu, 3, 8, n_ctas=sms)
     cyc = _median(L.fmha_microbench_alu, 3, 256, n_ctas=sms)
     out["softmax_exp_loop_cycles_per_128_scores"] = cyc / 256
+    # exp-loop variants: cycles per 128-score row (per warp slot)
+    loop = {}
+    for variant, name in ((0, "fma_ex2_sum_pack"), (1, "fma_ex2_sum"), (2, "ex2_sum"), (3, "fma_sum_pack"),
+                          (4, "fma_ex2_sum_alu_pack"), (5, "fma_ex2_f16x2_sum_pack"),
+                          (6, "ex2_f16x2_only_64_per_row"), (7, "quarter_pairs_on_fma_pipe"),
+                          (8, "eighth_pairs_on_fma_pipe")):
+        for threads in (128, 256):
+            _median(L.fmha_microbench_exp_loop, variant, threads, 4, n_ctas=sms)
+            cyc = _median(L.fmha_microbench_exp_loop, variant, threads, 64, n_ctas=sms)
+            loop[f"{name}_{threads // 128}warp_per_subpartition"] = round(cyc / 64, 1)
+    out["exp_loop_cycles_per_row"] = loop
     mreps = 512
     rows = []
     for a_tmem, b_mn, n, issuers, uniform in MMA_CASES:
@@ -84,6 +101,25 @@ def main():
                      "cycles_per_mma_per_issuer": round(per_issuer, 1),
                      "flop_per_clk_per_sm": round(issuers * 2 * 128 * n * 16 / per_issuer)})
     out["mma"] = rows
+    # cycles per MMA from the slope between two run lengths (start-up and
+    # drain cancel)
+    mix = {}
+    for mode, name, per_round in ((0, "pv_then_qk_two_tiles", 32), (1, "qk_only_two_tiles", 16),
+                                  (2, "pv_only_two_tiles", 16), (3, "pv_then_qk_with_smem_writes", 32),
+                                  (4, "one_tile_with_tmem_ld_st", 16), (5, "one_tile", 16),
+                                  (6, "pv_then_qk_commit_every_8", 32), (7, "pv_then_qk_commit_every_mma", 32),
+                                  (8, "pv_then_qk_commit_every_32", 32), (9, "qk_one_tile_commit_every_8", 8)):
+        _median(L.fmha_microbench_mma_mix, mode, 8, n_ctas=sms)
+        c1 = _median(L.fmha_microbench_mma_mix, mode, 64, n_ctas=sms)
+        c2 = _median(L.fmha_microbench_mma_mix, mode, 192, n_ctas=sms)
+        mix[name] = {"slope": round((c2 - c1) / (128 * per_round), 1), "whole": round(c2 / (192 * per_round), 1)}
+    out["mma_stream_cycles_per_mma"] = mix
+    # issuing-thread cycles at a step boundary, after 16 MMAs in flight
+    bnd = {}
+    for mode, name in ((0, "commit_then_try_wait"), (1, "try_wait_only"), (2, "commit_only")):
+        _median(L.fmha_microbench_boundary, mode, 8, n_ctas=sms)
+        bnd[name] = round(_median(L.fmha_microbench_boundary, mode, 128, n_ctas=sms) / 128, 1)
+    out["step_boundary_cycles"] = bnd
     _median(L.fmha_microbench_tmem_ld, 16, n_ctas=sms)
     cyc = _median(L.fmha_microbench_tmem_ld, reps, n_ctas=sms)
     out["tmem_ld_bytes_per_clk_per_sm"] = reps * 4 * 32 * 32 * 4 / cyc

@@ -29,6 +29,7 @@ from . import workloads as wl
 TRACE_LIB = os.path.join(_build.PKG, "libfmha_trace.so")
 SLOTS = 2048
 TR_SOFTMAX, TR_MMA, TR_CORR, TR_LOAD = 16, 1040, 1300, 1600
+TR_OBS_LOAD, TR_OBS_STEP = 272, 784
 
 
 def load_trace_lib(flags=()):
@@ -98,6 +99,106 @@ def summarize_ctas(ctas: np.ndarray) -> dict:
             "exit_ns_min_med_max": q(ext), "lifetime_ns_min_med_max": q(ext - ent)}
 
 
+def per_tile(row: np.ndarray, nblk: int) -> dict:
+    """Per-tile medians of the hand-off chain, SM cycles.
+
+    notice: P hand-off -> MMA warp acquires it; gate: the later of the P
+    hand-off and the correction warps' arrival for the same step, relative to
+    the P hand-off (> 0: the correction warps arrived last); skew: the last
+    of the tile's four softmax warps to hand off P, relative to warp 0 (the
+    stamped one); busy: the MMA
+    warp was still issuing the other tile when P arrived (cycles from the P
+    hand-off to the end of that issue); s_latency: last MMA of the group
+    issued -> softmax sees S; v_wait: MMA warp waits for the V block after the
+    previous step's last group.
+    """
+    def sm(t, j, e):
+        return int(row[TR_SOFTMAX + t * 512 + j * 8 + e])
+
+    def mma(j, e):
+        return int(row[TR_MMA + j * 8 + e])
+
+    def corr(j, t, e):
+        return int(row[TR_CORR + j * 8 + t * 4 + e])
+
+    res = {}
+    for t in (0, 1):
+        d = {k: [] for k in ("notice", "gate", "skew", "busy", "issue_span", "s_latency", "softmax")}
+        for j in range(nblk):
+            if not sm(t, j, 0):
+                continue
+            p_at = sm(t, j, 4)
+            d["softmax"].append(p_at - sm(t, j, 0))
+            others = [sm(t, j, 4 + w) for w in (1, 2, 3) if sm(t, j, 4 + w)]
+            if others:
+                d["skew"].append(max(others) - p_at)
+            acq, issued = mma(j, 1 + 2 * t), mma(j, 2 + 2 * t)
+            if corr(j, t, 1):
+                d["gate"].append(corr(j, t, 1) - p_at)
+            # the group the MMA warp issued just before this one
+            prev = mma(j, 2) if t == 1 else (mma(j - 1, 4) if j > 0 else 0)
+            if prev:
+                d["busy"].append(prev - p_at)
+            if acq:
+                d["notice"].append(acq - p_at)
+                if issued:
+                    d["issue_span"].append(issued - acq)
+                    if j + 1 < nblk and sm(t, j + 1, 0):
+                        d["s_latency"].append(sm(t, j + 1, 0) - issued)
+        res[f"tile{t}"] = {k: (statistics.median(v) if v else None) for k, v in d.items()}
+    vw = [mma(j, 0) - mma(j - 1, 4) for j in range(1, nblk) if mma(j, 0) and mma(j - 1, 4)]
+    res["v_wait"] = statistics.median(vw) if vw else None
+    return res
+
+
+def setup_and_ring(row: np.ndarray, nblk: int) -> dict:
+    """Set-up phases (cycles from kernel entry), ring-load latency (issue ->
+    landed, from the observer warp), and per-step MMA completion."""
+    med = lambda v: statistics.median(v) if v else None  # noqa: E731
+    s = {i: int(row[i]) for i in range(7)}
+    out = {}
+    if s[2]:
+        out["setup"] = {name: (s[i] - s[2] if s[i] else None) for name, i in
+                        (("barriers_init", 3), ("copies_issued", 4), ("tmem_alloc", 5), ("pre_sync", 6),
+                         ("sync_done", 0))}
+        first = int(row[TR_SOFTMAX])
+        out["setup"]["first_S0"] = first - s[2] if first else None
+    landed = [int(row[TR_OBS_LOAD + i]) for i in range(2 * nblk)]
+    issued = [int(row[TR_LOAD + i]) for i in range(2 * nblk)]
+    if s[4] and landed[0]:
+        out["early_load_latency"] = [x - s[4] for x in landed[:4] if x]
+    out["ring_load_latency"] = med([landed[i] - issued[i] for i in range(4, 2 * nblk) if landed[i] and issued[i]])
+    # V_j landed relative to the MMA warp acquiring it (negative: it waited on other things)
+    out["v_landed_minus_acquired"] = med([landed[2 * j + 1] - int(row[TR_MMA + j * 8])
+                                          for j in range(nblk) if landed[2 * j + 1] and row[TR_MMA + j * 8]])
+    # MMA warp: last group issued -> step commit issued -> V_(j+1) acquired
+    out["step_commit_issue"] = med([int(row[TR_MMA + j * 8 + 5]) - int(row[TR_MMA + j * 8 + 4])
+                                    for j in range(nblk) if row[TR_MMA + j * 8 + 5] and row[TR_MMA + j * 8 + 4]])
+    out["after_commit_to_v"] = med([int(row[TR_MMA + (j + 1) * 8]) - int(row[TR_MMA + j * 8 + 5])
+                                    for j in range(nblk - 1) if row[TR_MMA + (j + 1) * 8] and row[TR_MMA + j * 8 + 5]])
+    # PV issue of tile t (acquired -> about to issue its QK^T)
+    for t in (0, 1):
+        out[f"pv_issue_t{t}"] = med([int(row[TR_MMA + j * 8 + 6 + t]) - int(row[TR_MMA + j * 8 + 1 + 2 * t])
+                                     for j in range(nblk) if row[TR_MMA + j * 8 + 6 + t] and row[TR_MMA + j * 8 + 1 + 2 * t]])
+    done = [int(row[TR_OBS_STEP + n]) for n in range(nblk + 1)]
+    # step commit n = j + 1 completes after the step's last group was issued
+    out["step_complete_after_issue"] = med([done[j + 1] - int(row[TR_MMA + j * 8 + 4])
+                                            for j in range(nblk) if done[j + 1] and row[TR_MMA + j * 8 + 4]])
+    ep = lambda i: int(row[1560 + i])  # noqa: E731
+    # (rows with more blocks than the trace keeps have no valid last step)
+    last = done[nblk] if 0 < nblk < 32 and done[nblk] else 0
+    if last:
+        out["epilogue_after_last_mma"] = {
+            "tile0_O_seen": ep(0) - last if ep(0) else None, "tile0_O_stored": ep(1) - last if ep(1) else None,
+            "tile1_O_seen": ep(4) - last if ep(4) else None, "tile1_O_staged": ep(6) - last if ep(6) else None,
+            "tile1_O_stored": ep(5) - last if ep(5) else None,
+            "final_sync": ep(8) - last if ep(8) else None}
+        lastP = [int(row[TR_SOFTMAX + t * 512 + (nblk - 1) * 8 + 4]) for t in (0, 1)]
+        out["last_P_before_last_mma"] = [last - x if x else None for x in lastP]
+    out["step_period_in_pipe"] = med([done[n] - done[n - 1] for n in range(2, nblk + 1) if done[n] and done[n - 1]])
+    return out
+
+
 def summarize(row: np.ndarray) -> dict:
     """Median cycles per KV step of each phase, over both tiles and all steps."""
     t0 = row[0]
@@ -130,6 +231,8 @@ def summarize(row: np.ndarray) -> dict:
                 if issued:
                     ph["mma_issue_span"].append(issued - acq)
     out = {k: (statistics.median(v) if v else None) for k, v in ph.items()}
+    out["per_tile"] = per_tile(row, nblk)
+    out.update(setup_and_ring(row, nblk))
     out["blocks"] = nblk
     out["first_S_ready"] = sm(0, 0, 0) - int(t0) if sm(0, 0, 0) else None
     out["cta_end"] = int(row[1] - t0) if row[1] else None
