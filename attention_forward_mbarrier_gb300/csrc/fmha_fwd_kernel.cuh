@@ -102,7 +102,10 @@ constexpr int kWarpMma = 4 * kWgControl + 1;       // MMA issuer, TMEM owner
 // roles, for the timeout detail word
 constexpr int kRoleSoftmax = 1, kRoleCorrection = 2, kRoleLoad = 3, kRoleMma = 4, kRoleDrain = 5;
 
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
+#ifndef FMHA_WAIT_LIMIT_NS
+#define FMHA_WAIT_LIMIT_NS 1000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = FMHA_WAIT_LIMIT_NS;  // per wait (1 s by default)
 #ifndef FMHA_WAIT_HINT_NS
 #define FMHA_WAIT_HINT_NS 0
 #endif
@@ -650,7 +653,12 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
               if (t != t_last) ptx::mma_commit(ctx.bar(kBarSFull0));
             }
           }
+#ifndef FMHA_TEST_DROP_STEP_COMMIT
           ptx::mma_commit(ctx.bar(kBarStepDone + 0));  // step commit 0
+#else
+          // test build only: step commit 0 is never made, so the waits on it
+          // expire and the kernel must report a timeout and shut down cleanly
+#endif
           issued_any = true;
           for (int j = 0; j < n_kv && ok; ++j) {
             const int vidx = 2 * j + 1, vslot = vidx % kStages;
