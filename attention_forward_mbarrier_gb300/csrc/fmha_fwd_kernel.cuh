@@ -276,6 +276,13 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // first: start the descriptor fetches, which need no parameter loads, so
+  // they overlap the (cold) loads of the scalar parameters below
+  if (warp == kWarpProducer && lane == 0) {
+    ptx::prefetch_tensormap(&p.tmap_q);
+    ptx::prefetch_tensormap(&p.tmap_k);
+    ptx::prefetch_tensormap(&p.tmap_v);
+  }
 #ifdef FMHA_TRACE
   const size_t cta_lin = blockIdx.x + static_cast<size_t>(gridDim.x) * (blockIdx.y + static_cast<size_t>(gridDim.y) * blockIdx.z);
   unsigned long long* trace_row = (g_trace != nullptr && blockIdx.x == 0 && blockIdx.z == 0)
@@ -369,9 +376,6 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     ptx::fence_mbar_init();
     FMHA_TRACE_AT(3);
     // start the first copies now: they overlap the TMEM allocation and the sync
-    ptx::prefetch_tensormap(&p.tmap_q);
-    ptx::prefetch_tensormap(&p.tmap_k);
-    ptx::prefetch_tensormap(&p.tmap_v);
     // what the first S needs first (Q_0, K_0), then the rest: at launch every
     // CTA loads at once and DRAM bandwidth orders the arrivals
     const uint64_t pol_q = ptx::policy_evict_first();
