@@ -15,8 +15,9 @@
 //                   the running max, fold scale and -max into one packed FMA,
 //                   ex2, row sum, convert P to bf16 and tcgen05.st it over S;
 //                   then the tile's epilogue (O / l -> bf16 global, LSE);
-//   warpgroup 2     correction: rescales the O accumulator in TMEM when a row
-//                   max moved;
+//                   when a row max moved past the lazy threshold the softmax
+//                   warps rescale their own O rows in TMEM;
+//   warpgroup 2     idle (its registers go to the softmax warpgroups);
 //   warp 12         TMA producer: Q tiles once, then a K/V ring in shared
 //                   memory whose slots the MMA warp's step commits free;
 //   warp 13         MMA issuer: tcgen05.mma S = Q K^T (both operands in
@@ -55,10 +56,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kTiles * kTileBytes;
 constexpr uint32_t kOffBar = kOffKV + kStages * kTileBytes;
-constexpr uint32_t kNumBars = 16;
+constexpr uint32_t kNumBars = 14;
 constexpr uint32_t kOffMisc = kOffBar + 256;   // tmem base slot, abort flag
-constexpr uint32_t kOffAlpha = kOffBar + 512;  // float [2][128]
-constexpr uint32_t kSmemUsed = kOffAlpha + 1024;
+constexpr uint32_t kSmemUsed = kOffBar + 512;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kNumBars * 8 <= 256, "barrier area");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -73,10 +73,9 @@ constexpr int kBarQFull = 0;     // [2]
 constexpr int kBarKVFull = 2;    // [kStages]
 constexpr int kBarStepDone = 6;  // [2]  step commit n, alternating
 constexpr int kBarSFull0 = 8;    //      QK^T of tile 0 landed (tile 0 not the last tile)
-constexpr int kBarPVReady = 9;   // [2]  P stored and O corrected for tile t
-constexpr int kBarAlpha = 11;    // [2]  softmax published this block's alpha
-constexpr int kBarOFinal = 13;   // [2]  last PV of tile t complete
-constexpr int kBarMmaDone = 15;  //      every MMA retired
+constexpr int kBarPVReady = 9;   // [2]  P of tile t stored (and its O rows rescaled)
+constexpr int kBarOFinal = 11;   // [2]  last PV of tile t complete
+constexpr int kBarMmaDone = 13;  //      every MMA retired
 static_assert(kBarMmaDone + 1 == static_cast<int>(kNumBars), "ids");
 
 // bf16 packing of P: cvt.rn (round to nearest even, default) or integer
@@ -95,12 +94,12 @@ static_assert(kBarMmaDone + 1 == static_cast<int>(kNumBars), "ids");
 #endif
 constexpr int kWgControl = FMHA_CONTROL_FIRST ? 0 : 3;
 constexpr int kWgSoftmax0 = FMHA_CONTROL_FIRST ? 1 : 0;  // softmax of tile 0; tile 1 is the next warpgroup
-constexpr int kWgCorrection = FMHA_CONTROL_FIRST ? 3 : 2;
+constexpr int kWgIdle = FMHA_CONTROL_FIRST ? 3 : 2;
 constexpr int kWarpProducer = 4 * kWgControl;      // TMA producer, barrier set-up
 constexpr int kWarpMma = 4 * kWgControl + 1;       // MMA issuer, TMEM owner
 
 // roles, for the timeout detail word
-constexpr int kRoleSoftmax = 1, kRoleCorrection = 2, kRoleLoad = 3, kRoleMma = 4, kRoleDrain = 5;
+constexpr int kRoleSoftmax = 1, kRoleLoad = 3, kRoleMma = 4, kRoleDrain = 5;
 
 #ifndef FMHA_WAIT_LIMIT_NS
 #define FMHA_WAIT_LIMIT_NS 1000000000ull
@@ -117,8 +116,10 @@ constexpr uint32_t kWaitHintNs = FMHA_WAIT_HINT_NS;
 // Register budgets per warpgroup after the split (sum x 128 threads = 64K).
 // Helper calls in these regions must be inlined: ptxas cannot place an ABI
 // call inside a setmaxnreg region.
-constexpr int kRegsSoftmax = 192, kRegsCorrection = 48, kRegsControl = 80;
-static_assert(2 * kRegsSoftmax + kRegsCorrection + kRegsControl == 512, "register split");
+// Warpgroup 2 has no work (the softmax warps rescale their own O rows) and
+// gives its registers to the softmax.
+constexpr int kRegsSoftmax = 200, kRegsIdle = 32, kRegsControl = 80;
+static_assert(2 * kRegsSoftmax + kRegsIdle + kRegsControl == 512, "register split");
 
 struct alignas(64) FwdParams {
   CUtensorMap tmap_q;  // [total_q, heads*128] bf16, box 64 x 128, 128B swizzle
@@ -143,7 +144,6 @@ __device__ int g_status;  // 0 = ok, else 1 + (role * 256 + barrier id) of the f
 constexpr int kTraceSlots = 2048;
 constexpr int kTrSoftmax = 16;      // + t * 512 + j * 8 + event
 constexpr int kTrMma = 1040;        // + j * 8 + event
-constexpr int kTrCorrection = 1300; // + j * 8 + t * 4 + event
 constexpr int kTrLoad = 1600;       // + ring index
 constexpr int kTrMaxBlocks = 32;
 constexpr int kTrObsLoad = 272;  // + ring index (< 256): ring load landed
@@ -267,6 +267,49 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint6
     ptx::mma_ts_imm<true>(tmem_d, tmem_p + 8u * k, v_desc + ((2048u * k) >> 4), idesc);
 }
 
+// Row max of 128 scores: three-input max, four independent chains.  (The
+// max is bound by min/max throughput, ~250 cycles a row: more chains or a
+// two-input tree measured no faster.)
+__device__ __forceinline__ float row_max128(const float (&s)[128]) {
+  float mx[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float a = ptx::fmax3(s[32 * q + 0], s[32 * q + 1], s[32 * q + 2]);
+#pragma unroll
+    for (int k = 3; k < 31; k += 2) a = ptx::fmax3(a, s[32 * q + k], s[32 * q + k + 1]);
+    mx[q] = fmaxf(a, s[32 * q + 31]);
+  }
+  return ptx::fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+}
+
+// One softmax exp pass over a row of 128 scores with reference max m_ref:
+// P = 2^(s c - m_ref c) (one packed FMA per pair, ex2), bf16 pairs stored to
+// TMEM at t_s (64 columns); returns the row sum of P.
+__device__ __forceinline__ float exp_pass(const float (&s)[128], float c, float m_ref, uint32_t t_s) {
+  const float neg_mc = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
+  const float2 c2 = make_float2(c, c);
+  const float2 nm2 = make_float2(neg_mc, neg_mc);
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int k = half * 64 + 2 * i;
+      const float2 x = __ffma2_rn(make_float2(s[k], s[k + 1]), c2, nm2);
+      const float p0 = ptx::ex2_approx(x.x);
+      const float p1 = ptx::ex2_approx(x.y);
+      acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
+      pk[i] = FMHA_P_PACK(p0, p1);
+    }
+    ptx::tmem_st32(t_s + 32u * half, pk);
+  }
+  const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+  const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+  const float2 a = __fadd2_rn(a01, a23);
+  return a.x + a.y;
+}
+
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -333,7 +376,6 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
   ctx.bar0 = base + kOffBar;
   ctx.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  float* s_alpha = reinterpret_cast<float*>(smem + kOffAlpha);
 
   // TMA producer steps (one thread): the Q tiles, and ring load idx = K (even) or
   // V (odd) of key block idx / 2 into slot idx % kStages.
@@ -365,8 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     for (int t = 0; t < kTiles; ++t) {
       ptx::mbar_init(ctx.bar(kBarQFull + t), 1);
       ptx::mbar_init(ctx.bar(kBarStepDone + t), 1);
-      ptx::mbar_init(ctx.bar(kBarPVReady + t), 8);  // 4 softmax warps + 4 correction warps
-      ptx::mbar_init(ctx.bar(kBarAlpha + t), 4);    // 4 softmax warps
+      ptx::mbar_init(ctx.bar(kBarPVReady + t), 4);  // the tile's 4 softmax warps
       ptx::mbar_init(ctx.bar(kBarOFinal + t), 1);
     }
     for (int s = 0; s < kStages; ++s) ptx::mbar_init(ctx.bar(kBarKVFull + s), 1);
@@ -435,51 +476,31 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         for (int k = 0; k < 128; ++k)
           if (k >= lim) s[k] = -INFINITY;
       }
-      float mx[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float a = ptx::fmax3(s[32 * q + 0], s[32 * q + 1], s[32 * q + 2]);
-#pragma unroll
-        for (int k = 3; k < 31; k += 2) a = ptx::fmax3(a, s[32 * q + k], s[32 * q + k + 1]);
-        mx[q] = fmaxf(a, s[32 * q + 31]);
-      }
-      const float m_blk = ptx::fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
-      const float m_new = fmaxf(m_used, m_blk);
-      float alpha = 1.f;
-      // rescale only when the max grew by more than the threshold (NaN when both are -inf: skip)
-      if ((m_new - m_used) * c > p.rescale_threshold) {
-        alpha = ptx::ex2_approx((m_used - m_new) * c);  // m_used == -inf gives 0
-        m_used = m_new;
-      }
-      s_alpha[t * 128 + r] = alpha;
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarAlpha + t));
+      // block max; the max in use moves only when it grew by more than the
+      // threshold (lazy rescale; NaN when both are -inf: keep)
+      const float m_blk = row_max128(s);
+      const float m_ref = (m_blk - m_used) * c > p.rescale_threshold ? m_blk : m_used;
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 2);
-
-      const float neg_mc = (m_used == -INFINITY) ? 0.f : -m_used * c;
-      const float2 c2 = make_float2(c, c);
-      const float2 nm2 = make_float2(neg_mc, neg_mc);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int k = half * 64 + 2 * i;
-          const float2 x = __ffma2_rn(make_float2(s[k], s[k + 1]), c2, nm2);
-          const float p0 = ptx::ex2_approx(x.x);
-          const float p1 = ptx::ex2_approx(x.y);
-          acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
-          pk[i] = FMHA_P_PACK(p0, p1);
-        }
-        ptx::tmem_st32(t_s + 32u * half, pk);
-      }
-      const float2 a01 = __fadd2_rn(acc[0], acc[1]);
-      const float2 a23 = __fadd2_rn(acc[2], acc[3]);
-      const float2 a = __fadd2_rn(a01, a23);
-      l = l * alpha + (a.x + a.y);
+      const float row_sum = exp_pass(s, c, m_ref, t_s);
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 3);
+      // m_used == -inf gives alpha 0 (its O rows and l are still 0)
+      const float alpha = (m_ref == m_used) ? 1.f : ptx::ex2_approx((m_used - m_ref) * c);
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // Rescale this warp's O rows.  PV_t(j-1) has completed (S_t(j) is
+        // committed after it) and PV_t(j) waits for this warp's P hand-off.
+        const uint32_t t_o = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16) + col_o(t);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          ptx::tmem_ld32_wait(t_o + 32u * cc, o);
+          uint32_t u[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(o[i] * alpha);
+          ptx::tmem_st32(t_o + 32u * cc, u);
+        }
+      }
+      l = l * alpha + row_sum;
+      m_used = m_ref;
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
@@ -568,45 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       }
       if (r == 0) FMHA_TRACE_AT(kTrEpilogue + 4 * t + 1);
     }
-  } else if (wg == kWgCorrection) {
-    // =============================== correction
-    ptx::setmaxnreg_dec<kRegsCorrection>();
-    const int r = (warp & 3) * 32 + lane;
-    const uint32_t lane_base = (static_cast<uint32_t>(warp & 3) * 32u) << 16;
-    bool ok = true;
-    for (int j = 0; j < n_kv && ok; ++j) {
-#pragma unroll
-      for (int t = 0; t < kTiles; ++t) {
-        if (!ok) break;
-        const uint32_t t_o = tmem + lane_base + col_o(t);
-        if (j < n_blk(t)) {
-          if (!wait_bar_warp(ctx, kBarAlpha + t, j & 1, kRoleCorrection)) {
-            ok = false;
-            break;
-          }
-          const bool tr = (r == 0 && j < kTrMaxBlocks);
-          if (tr) FMHA_TRACE_AT(kTrCorrection + j * 8 + t * 4 + 0);
-          const float alpha = s_alpha[t * 128 + r];
-          if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-            ptx::tc_fence_after();
-#pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-              float o[32];
-              ptx::tmem_ld32_wait(t_o + 32u * cc, o);
-              uint32_t u[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(o[i] * alpha);
-              ptx::tmem_st32(t_o + 32u * cc, u);
-            }
-            ptx::tmem_wait_st();
-          }
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVReady + t));
-          if (tr) FMHA_TRACE_AT(kTrCorrection + j * 8 + t * 4 + 1);
-        }
-      }
-    }
+  } else if (wg == kWgIdle) {
+    // =============================== idle (its registers go to the softmax)
+    ptx::setmaxnreg_dec<kRegsIdle>();
   } else {
     ptx::setmaxnreg_dec<kRegsControl>();
     if (warp == kWarpProducer) {
@@ -739,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
   }
 
 #ifdef FMHA_TRACE
-  if (warp == 4 * kWgCorrection && lane == 0) FMHA_TRACE_AT(1);
+  if (warp == 4 * kWgIdle && lane == 0) FMHA_TRACE_AT(1);
 #endif
   ptx::tc_fence_before();
   __syncthreads();

@@ -337,7 +337,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) mma_probe(int issuers, int reps
 // Issuing-thread cost of the step boundary: each round issues the 16 MMAs of
 // one tile group (8 PV + 8 QK^T), then mode 0: tcgen05.commit then
 // mbarrier.try_wait on an already-completed barrier; 1: the try_wait alone;
-// 2: the commit alone.  Returns the summed cycles of that boundary sequence.
+// 2: the commit alone.  Modes 3-5: the same three after 16 MMAs of N=256
+// (128 cycles each, so more work is still in flight at the boundary).
+// Returns the summed cycles of that boundary sequence.
 template <int mode>
 __global__ void __launch_bounds__(kTcThreads, 1) boundary_probe(int reps, long long* out, int* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -356,19 +358,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) boundary_probe(int reps, long l
     const uint64_t k0 = ptx::smem_desc_sw128(base + kMbB, 16, 1024);
     const uint64_t v0 = ptx::smem_desc_sw128(base + kMbB + 32768u, 16384, 1024);
     int fails = 0;
+    const uint32_t id_wide = ptx::idesc_bf16_f32(128, 256, false, false);
     for (int r = 0; r < reps; ++r) {
+      if (mode < 3) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        ptx::mma_ts(tmem + 256u, tmem + 8u * k, v0 + ((2048u * k) >> 4), id_pv, 1u);
+        for (int k = 0; k < 8; ++k)
+          ptx::mma_ts(tmem + 256u, tmem + 8u * k, v0 + ((2048u * k) >> 4), id_pv, 1u);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint64_t off = ((k >> 2) * 16384u + (k & 3) * 32u) >> 4;
-        ptx::mma_ss(tmem, q0 + off, k0 + off, id_qk, k > 0 ? 1u : 0u);
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t off = ((k >> 2) * 16384u + (k & 3) * 32u) >> 4;
+          ptx::mma_ss(tmem, q0 + off, k0 + off, id_qk, k > 0 ? 1u : 0u);
+        }
+      } else {
+        // D = columns [0, 256); B = 256 K-major rows (the whole 64 KiB B tile)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const uint64_t a_off = (((k & 7) >> 2) * 16384u + (k & 3) * 32u) >> 4;
+          const uint64_t b_off = (((k & 7) >> 2) * 32768u + (k & 3) * 32u) >> 4;
+          ptx::mma_ss(tmem, q0 + a_off, k0 + b_off, id_wide, k > 0 ? 1u : 0u);
+        }
       }
       long long a, b;
       asm volatile("mov.u64 %0, %%clock64;" : "=l"(a)::"memory");
-      if (mode != 1) ptx::mma_commit(base + kMbBar + 8u);
-      if (mode != 2 && !ptx::mbar_try_wait(done_bar, 0)) ++fails;
+      if (mode != 1 && mode != 4) ptx::mma_commit(base + kMbBar + 8u);
+      if (mode != 2 && mode != 5 && !ptx::mbar_try_wait(done_bar, 0)) ++fails;
       asm volatile("mov.u64 %0, %%clock64;" : "=l"(b)::"memory");
       acc += b - a;
     }
@@ -622,7 +635,7 @@ extern "C" int fmha_microbench_mma_mix(int mode, int reps, long long* out_cycles
 // Summed cycles of the step-boundary sequence of boundary_probe over `reps`
 // rounds.  Returns as fmha_microbench_mma.
 extern "C" int fmha_microbench_boundary(int mode, int reps, long long* out_cycles, int n_ctas) {
-  if (mode < 0 || mode > 2 || reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
+  if (mode < 0 || mode > 5 || reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
   long long* d_out = nullptr;
   int* d_status = nullptr;
   if (!alloc(&d_out, &d_status, n_ctas)) return 2;
@@ -633,7 +646,10 @@ extern "C" int fmha_microbench_boundary(int mode, int reps, long long* out_cycle
   switch (mode) {
     case 0: launch(boundary_probe<0>); break;
     case 1: launch(boundary_probe<1>); break;
-    default: launch(boundary_probe<2>); break;
+    case 2: launch(boundary_probe<2>); break;
+    case 3: launch(boundary_probe<3>); break;
+    case 4: launch(boundary_probe<4>); break;
+    default: launch(boundary_probe<5>); break;
   }
   return finish(d_out, d_status, nullptr, out_cycles, n_ctas);
 }

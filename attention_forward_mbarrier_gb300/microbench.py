@@ -116,7 +116,8 @@ def main():
     out["mma_stream_cycles_per_mma"] = mix
     # issuing-thread cycles at a step boundary, after 16 MMAs in flight
     bnd = {}
-    for mode, name in ((0, "commit_then_try_wait"), (1, "try_wait_only"), (2, "commit_only")):
+    for mode, name in ((0, "commit_then_try_wait"), (1, "try_wait_only"), (2, "commit_only"),
+                       (3, "n256_commit_then_try_wait"), (4, "n256_try_wait_only"), (5, "n256_commit_only")):
         _median(L.fmha_microbench_boundary, mode, 8, n_ctas=sms)
         bnd[name] = round(_median(L.fmha_microbench_boundary, mode, 128, n_ctas=sms) / 128, 1)
     out["step_boundary_cycles"] = bnd

@@ -28,7 +28,7 @@ from . import workloads as wl
 
 TRACE_LIB = os.path.join(_build.PKG, "libfmha_trace.so")
 SLOTS = 2048
-TR_SOFTMAX, TR_MMA, TR_CORR, TR_LOAD = 16, 1040, 1300, 1600
+TR_SOFTMAX, TR_MMA, TR_LOAD = 16, 1040, 1600
 TR_OBS_LOAD, TR_OBS_STEP = 272, 784
 
 
@@ -58,7 +58,10 @@ def run(w: wl.Workload, repeats: int = 3, flags=(), flush_l2: bool = True):
     pairs = (w.max_seqlen_q + 255) // 256
     buf = torch.zeros((pairs, SLOTS), dtype=torch.int64, device=dev)
     ctas = torch.zeros((w.heads * pairs * w.batch, 4), dtype=torch.int64, device=dev)
-    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    # the benchmark's L2 flush: write 504 MiB, then read another 504 MiB
+    flush = torch.empty(126 * 1024 * 1024, dtype=torch.float32, device=dev)
+    reader = torch.zeros(126 * 1024 * 1024, dtype=torch.float32, device=dev) if flush_l2 else None
+    sink = torch.empty(1, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream().cuda_stream
 
     def ptr(t):
@@ -72,6 +75,7 @@ def run(w: wl.Workload, repeats: int = 3, flags=(), flush_l2: bool = True):
             ctas.zero_()
             if flush_l2:
                 flush.zero_()  # the benchmark's L2 flush precedes every launch
+                sink.copy_(reader.sum().reshape(1))
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             st = L.fmha_fwd(ptr(q), ptr(k), ptr(v), ptr(out), ptr(lse), ptr(cq), ptr(ck), w.batch,
@@ -102,9 +106,7 @@ def summarize_ctas(ctas: np.ndarray) -> dict:
 def per_tile(row: np.ndarray, nblk: int) -> dict:
     """Per-tile medians of the hand-off chain, SM cycles.
 
-    notice: P hand-off -> MMA warp acquires it; gate: the later of the P
-    hand-off and the correction warps' arrival for the same step, relative to
-    the P hand-off (> 0: the correction warps arrived last); skew: the last
+    notice: P hand-off -> MMA warp acquires it; skew: the last
     of the tile's four softmax warps to hand off P, relative to warp 0 (the
     stamped one); busy: the MMA
     warp was still issuing the other tile when P arrived (cycles from the P
@@ -118,12 +120,9 @@ def per_tile(row: np.ndarray, nblk: int) -> dict:
     def mma(j, e):
         return int(row[TR_MMA + j * 8 + e])
 
-    def corr(j, t, e):
-        return int(row[TR_CORR + j * 8 + t * 4 + e])
-
     res = {}
     for t in (0, 1):
-        d = {k: [] for k in ("notice", "gate", "skew", "busy", "issue_span", "s_latency", "softmax")}
+        d = {k: [] for k in ("notice", "skew", "busy", "issue_span", "s_latency", "softmax")}
         for j in range(nblk):
             if not sm(t, j, 0):
                 continue
@@ -133,8 +132,6 @@ def per_tile(row: np.ndarray, nblk: int) -> dict:
             if others:
                 d["skew"].append(max(others) - p_at)
             acq, issued = mma(j, 1 + 2 * t), mma(j, 2 + 2 * t)
-            if corr(j, t, 1):
-                d["gate"].append(corr(j, t, 1) - p_at)
             # the group the MMA warp issued just before this one
             prev = mma(j, 2) if t == 1 else (mma(j - 1, 4) if j > 0 else 0)
             if prev:
