@@ -41,6 +41,11 @@ class Workload:
     causal: bool
     dense: bool = False  # True: equal lengths, passed without cu_seqlens
     scale: Optional[float] = None  # None -> 1/sqrt(head_dim)
+    kv_heads: Optional[int] = None  # grouped K/V heads; None -> heads (multi-head)
+
+    @property
+    def n_kv_heads(self) -> int:
+        return self.heads if self.kv_heads is None else int(self.kv_heads)
 
     @property
     def batch(self) -> int:
@@ -99,19 +104,21 @@ def linspace_docs(total: int, docs: int) -> tuple:
 
 
 def dense(name, batch, seqlen_q, heads, head_dim=128, causal=False, seqlen_k=None,
-          description="", scale=None) -> Workload:
+          description="", scale=None, kv_heads=None) -> Workload:
     seqlen_k = seqlen_q if seqlen_k is None else seqlen_k
     return Workload(name, description, heads, head_dim, (seqlen_q,) * batch,
-                    (seqlen_k,) * batch, causal, dense=True, scale=scale)
+                    (seqlen_k,) * batch, causal, dense=True, scale=scale, kv_heads=kv_heads)
 
 
 def varlen(name, seqlens_q: Sequence[int], heads, head_dim=128, causal=True,
-           seqlens_k: Optional[Sequence[int]] = None, description="", scale=None) -> Workload:
+           seqlens_k: Optional[Sequence[int]] = None, description="", scale=None,
+           kv_heads=None) -> Workload:
     seqlens_k = seqlens_q if seqlens_k is None else seqlens_k
     if len(seqlens_k) != len(seqlens_q):
         raise ValueError("seqlens_q and seqlens_k must have the same number of sequences")
     return Workload(name, description, heads, head_dim, tuple(int(x) for x in seqlens_q),
-                    tuple(int(x) for x in seqlens_k), causal, dense=False, scale=scale)
+                    tuple(int(x) for x in seqlens_k), causal, dense=False, scale=scale,
+                    kv_heads=kv_heads)
 
 
 # The five named workloads.
@@ -156,8 +163,8 @@ def make_inputs(w: Workload, seed: int = 0, dist: str = "randn") -> Inputs:
     """
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
-    shapes = [(w.total_q, w.heads, w.head_dim), (w.total_k, w.heads, w.head_dim),
-              (w.total_k, w.heads, w.head_dim)]
+    shapes = [(w.total_q, w.heads, w.head_dim), (w.total_k, w.n_kv_heads, w.head_dim),
+              (w.total_k, w.n_kv_heads, w.head_dim)]
     out = []
     for shp in shapes:
         if dist == "randn":

@@ -64,7 +64,8 @@ def _load(path: str = _LIB_PATH):
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,  # cu_q cu_k batch
         ctypes.c_int64, ctypes.c_int64,  # total_q total_k
         ctypes.c_int, ctypes.c_int,  # max_seqlen_q max_seqlen_k
-        ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,  # heads head_dim scale causal
+        ctypes.c_int, ctypes.c_int, ctypes.c_int,  # heads kv_heads head_dim
+        ctypes.c_double, ctypes.c_int,  # scale causal
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,  # rows n_rows n_threads
     ]
     lib.oracle_num_threads.restype = ctypes.c_int
@@ -122,7 +123,8 @@ def oracle_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seq
     """fp64 attention forward from the C oracle.
 
     q: [total_q, heads, head_dim] bf16 (numpy uint16 bits or torch bf16),
-    k, v: [total_k, heads, head_dim].  cu_seqlens_q / cu_seqlens_k: int32
+    k, v: [total_k, kv_heads, head_dim] (kv_heads divides heads; query head h
+    reads K/V head h // (heads // kv_heads)).  cu_seqlens_q / cu_seqlens_k: int32
     prefix offsets of length batch+1, or None for dense batches.
     rows: optional int64 array of flattened (token * heads + head) indices.
     lib_handle: a library from ``load_variant`` (tests build deliberately
@@ -134,9 +136,9 @@ def oracle_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seq
     if qb.ndim != 3:
         raise ValueError("q must be [tokens, heads, head_dim]")
     total_q, heads, head_dim = qb.shape
-    total_k = kb.shape[0]
-    if kb.shape[1:] != (heads, head_dim) or vb.shape != kb.shape:
-        raise ValueError("k and v must be [total_k, heads, head_dim]")
+    total_k, kv_heads = kb.shape[0], kb.shape[1]
+    if kb.ndim != 3 or kb.shape[2] != head_dim or vb.shape != kb.shape or heads % kv_heads != 0:
+        raise ValueError("k and v must be [total_k, kv_heads, head_dim] with kv_heads dividing heads")
     if (cu_seqlens_q is None) != (cu_seqlens_k is None):
         raise ValueError("cu_seqlens_q and cu_seqlens_k must both be given or both be None")
     cu_q = cu_k = None
@@ -160,7 +162,7 @@ def oracle_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seq
         cu_q.ctypes.data if cu_q is not None else None,
         cu_k.ctypes.data if cu_k is not None else None,
         int(batch), int(total_q), int(total_k), int(max_seqlen_q), int(max_seqlen_k),
-        int(heads), int(head_dim), float(scale), int(bool(causal)),
+        int(heads), int(kv_heads), int(head_dim), float(scale), int(bool(causal)),
         rows_arr.ctypes.data if rows_arr is not None else None, int(n_rows), int(n_threads))
     if rc != 0:
         raise ValueError("oracle_fmha_fwd rejected its arguments")
@@ -180,6 +182,7 @@ def brute_force_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, ma
     """
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     total_q, heads, head_dim = qb.shape
+    group = heads // kb.shape[1]  # query heads per K/V head
     to_f = np.vectorize(_bf16_bits_to_float, otypes=[float])
     Q, K, V = to_f(qb).tolist(), to_f(kb).tolist(), to_f(vb).tolist()
     out = [[[0.0] * head_dim for _ in range(heads)] for _ in range(total_q)]
@@ -198,13 +201,13 @@ def brute_force_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, ma
                         continue
                     dot = 0.0
                     for d in range(head_dim):
-                        dot += Q[q0 + i][h][d] * K[k0 + j][h][d]
+                        dot += Q[q0 + i][h][d] * K[k0 + j][h // group][d]
                     weights.append((j, math.exp(scale * dot)))
                 if not weights:
                     lse[h][q0 + i] = -math.inf
                     continue
                 z = sum(w for _, w in weights)
                 for d in range(head_dim):
-                    out[q0 + i][h][d] = sum(w * V[k0 + j][h][d] for j, w in weights) / z
+                    out[q0 + i][h][d] = sum(w * V[k0 + j][h // group][d] for j, w in weights) / z
                 lse[h][q0 + i] = math.log(z)
     return np.array(out, dtype=np.float64), np.array(lse, dtype=np.float64)

@@ -28,6 +28,11 @@
  * diagonal to the bottom-right (j <= i + Lk - Lq).  A row with no visible key
  * gets O = 0 and LSE = -inf.
  *
+ * Grouped K/V heads (not on the pages; the plainest extension): with kv_heads
+ * K/V heads for heads query heads (heads a multiple of kv_heads), query head h
+ * reads K/V head h / (heads / kv_heads), i.e. consecutive query heads share
+ * one K/V head.  kv_heads == heads is ordinary multi-head attention.
+ *
  * Inputs are bf16 bit patterns (uint16), upcast exactly to double.
  */
 #include <math.h>
@@ -70,11 +75,13 @@ static void doc_bounds(const int32_t *cu_q, const int32_t *cu_k, int b,
  */
 static void oracle_row(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                        int64_t q0, int64_t lq, int64_t k0, int64_t lk,
-                       int64_t i, int h, int heads, int head_dim, double scale,
-                       int causal, double *s_buf, char *mask_buf,
+                       int64_t i, int h, int heads, int kv_heads, int head_dim,
+                       double scale, int causal, double *s_buf, char *mask_buf,
                        double *o_row, double *lse_out)
 {
     const int64_t row_stride = (int64_t)heads * head_dim;
+    const int64_t kv_stride = (int64_t)kv_heads * head_dim;
+    const int hk = h / (heads / kv_heads); /* this query head's K/V head */
     const uint16_t *qi = q + (q0 + i) * row_stride + (int64_t)h * head_dim;
 
     /* explicit mask row */
@@ -83,7 +90,7 @@ static void oracle_row(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 
     /* all scores, then the mask */
     for (int64_t j = 0; j < lk; ++j) {
-        const uint16_t *kj = k + (k0 + j) * row_stride + (int64_t)h * head_dim;
+        const uint16_t *kj = k + (k0 + j) * kv_stride + (int64_t)hk * head_dim;
         double dot = 0.0;
         for (int d = 0; d < head_dim; ++d)
             dot += bf16_bits_to_double(qi[d]) * bf16_bits_to_double(kj[d]);
@@ -114,7 +121,7 @@ static void oracle_row(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     for (int64_t j = 0; j < lk; ++j) {
         if (s_buf[j] == 0.0)
             continue;
-        const uint16_t *vj = v + (k0 + j) * row_stride + (int64_t)h * head_dim;
+        const uint16_t *vj = v + (k0 + j) * kv_stride + (int64_t)hk * head_dim;
         for (int d = 0; d < head_dim; ++d)
             o_row[d] += s_buf[j] * bf16_bits_to_double(vj[d]);
     }
@@ -135,7 +142,8 @@ static int doc_of_token(const int32_t *cu_q, int batch, int64_t tok)
 /*
  * oracle_fmha_fwd
  *
- * q, k, v : bf16 bits, [total_q | total_k, heads, head_dim] contiguous.
+ * q       : bf16 bits, [total_q, heads, head_dim] contiguous.
+ * k, v    : bf16 bits, [total_k, kv_heads, head_dim] contiguous.
  * cu_q/cu_k : int32 prefix offsets [batch + 1], or both NULL for dense
  *             batches of max_seqlen_q / max_seqlen_k rows each.
  * rows == NULL : full output.  out is [total_q, heads, head_dim] double and
@@ -150,11 +158,13 @@ int oracle_fmha_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                     const int32_t *cu_q, const int32_t *cu_k, int batch,
                     int64_t total_q, int64_t total_k,
                     int max_seqlen_q, int max_seqlen_k,
-                    int heads, int head_dim, double scale, int causal,
+                    int heads, int kv_heads, int head_dim, double scale, int causal,
                     const int64_t *rows, int64_t n_rows, int n_threads)
 {
     (void)total_k;
     if (!q || !k || !v || !out || !lse || batch < 0 || heads < 1 || head_dim < 1)
+        return -1;
+    if (kv_heads < 1 || heads % kv_heads != 0)
         return -1;
     if ((cu_q == NULL) != (cu_k == NULL))
         return -1;
@@ -204,8 +214,8 @@ int oracle_fmha_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             int64_t q0, lq, k0, lk;
             doc_bounds(cu_q, cu_k, b, max_seqlen_q, max_seqlen_k, &q0, &lq, &k0, &lk);
             double lse_val;
-            oracle_row(q, k, v, q0, lq, k0, lk, tok - q0, h, heads, head_dim, scale,
-                       causal, s_buf, mask_buf, o_row, &lse_val);
+            oracle_row(q, k, v, q0, lq, k0, lk, tok - q0, h, heads, kv_heads, head_dim,
+                       scale, causal, s_buf, mask_buf, o_row, &lse_val);
             double *dst = rows ? out + it * head_dim
                                : out + (tok * heads + h) * (int64_t)head_dim;
             memcpy(dst, o_row, sizeof(double) * (size_t)head_dim);

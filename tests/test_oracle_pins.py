@@ -15,8 +15,11 @@ implementation fixes:
                    permutation (non-causal), head permutation, K shift;
 * planted mistakes -- broken copies of the C source (dropped scale, causal
                    off-by-one, top-left alignment, LSE without the max, no
-                   normalisation, q used for k, wrong head) must each fail at
-                   least one pin.
+                   normalisation, q used for k, wrong head, K/V head by modulo
+                   instead of by group) must each fail at least one pin;
+* grouped K/V heads -- equal to multi-head attention with each K/V head
+                   repeated for its group of query heads, and the brute force
+                   on a tiny grouped shape.
 
 Definition being pinned: "[BUG] Unexpected Slower Performance in C++ CuTe
 (77_blackwell_fmha) vs Python CuTe DSL (fmha.py) on Jetson Thor", section
@@ -242,9 +245,31 @@ def pin_key_shift(fn):
     assert np.max(np.abs((l2 - l1)[0] - shift)) <= 1e-13
 
 
+def pin_grouped_kv_heads(fn):
+    # Grouped K/V heads: 6 query heads on 2 K/V heads must equal ordinary
+    # multi-head attention with each K/V head repeated for its 3 query heads
+    # (query head h reads K/V head h // 3).  Also the pure-Python brute force
+    # on a tiny grouped shape.
+    w = wl.varlen("gqa", (23, 40), 6, head_dim=16, causal=True, kv_heads=2)
+    inp = wl.make_inputs(w, seed=41)
+    out, lse = fn(*inp.oracle_args())
+    args = list(inp.oracle_args())
+    args[1] = inp.k.repeat_interleave(3, dim=1)
+    args[2] = inp.v.repeat_interleave(3, dim=1)
+    out2, lse2 = fn(*args)
+    assert_close(out, out2, 1e-13)
+    assert_close(lse, lse2, 1e-13)
+    wb = wl.varlen("gqa_bf", (9, 5), 4, head_dim=8, causal=False, seqlens_k=(7, 11), kv_heads=2)
+    ib = wl.make_inputs(wb, seed=43, dist="uniform")
+    a = fn(*ib.oracle_args())
+    b = oracle.brute_force_fwd(*ib.oracle_args())
+    assert_close(a[0], b[0])
+    assert_close(a[1], b[1])
+
+
 PINS = [pin_brute_force, pin_library, pin_scale_zero, pin_identical_keys, pin_causal_row0,
         pin_ones_v, pin_two_keys, pin_varlen_equals_alone, pin_key_permutation,
-        pin_head_permutation, pin_key_shift]
+        pin_head_permutation, pin_key_shift, pin_grouped_kv_heads]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -280,9 +305,10 @@ MUTANTS = {
     "no_normalisation": ("o_row[d] /= z;", "o_row[d] /= 1.0;"),
     "q_used_for_k": ("bf16_bits_to_double(qi[d]) * bf16_bits_to_double(kj[d])",
                      "bf16_bits_to_double(qi[d]) * bf16_bits_to_double(qi[d])"),
-    "wrong_head_for_v": ("const uint16_t *vj = v + (k0 + j) * row_stride + (int64_t)h * head_dim;",
-                         "const uint16_t *vj = v + (k0 + j) * row_stride;"),
+    "wrong_head_for_v": ("const uint16_t *vj = v + (k0 + j) * kv_stride + (int64_t)hk * head_dim;",
+                         "const uint16_t *vj = v + (k0 + j) * kv_stride;"),
     "max_not_subtracted": ("double p = exp(s_buf[j] - m);", "double p = exp(s_buf[j]);"),
+    "kv_head_modulo": ("const int hk = h / (heads / kv_heads);", "const int hk = h % kv_heads;"),
 }
 
 
