@@ -21,7 +21,7 @@ FMHA_ERR_TIMEOUT = 4
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfmha.so")
 
 # exported symbols, in the order include/fmha.h declares them
-SYMBOLS = ("fmha_fwd", "fmha_get_device_status", "fmha_status_string", "fmha_version")
+SYMBOLS = ("fmha_fwd", "fmha_fwd_gqa", "fmha_get_device_status", "fmha_status_string", "fmha_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -48,6 +48,13 @@ def lib():
                 ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p,
+            ]
+            L.fmha_fwd_gqa.restype = ctypes.c_int
+            L.fmha_fwd_gqa.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p,
             ]
             L.fmha_get_device_status.restype = ctypes.c_int
             L.fmha_get_device_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]
@@ -90,6 +97,15 @@ def fmha_fwd(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, tota
                               int(head_dim), float(scale), int(causal), _stream(stream)))
 
 
+def fmha_fwd_gqa(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                 max_seqlen_q, max_seqlen_k, heads, kv_heads, head_dim, scale, causal, stream=None) -> int:
+    """The grouped-K/V-head C entry point; tensors or raw pointers.  Returns the status."""
+    return int(lib().fmha_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                  _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(batch), int(total_q),
+                                  int(total_k), int(max_seqlen_q), int(max_seqlen_k), int(heads),
+                                  int(kv_heads), int(head_dim), float(scale), int(causal), _stream(stream)))
+
+
 def fmha_get_device_status(stream=None):
     """(status, detail): synchronises the stream and reads/clears the device status word."""
     detail = ctypes.c_int(0)
@@ -114,7 +130,8 @@ def attention_forward(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_
                       return_lse=True, stream=None):
     """Convenience wrapper over ``fmha_fwd`` for CUDA torch tensors.
 
-    q: [total_q, heads, 128] bf16 (or [b, s, heads, 128] dense), k/v likewise.
+    q: [total_q, heads, 128] bf16 (or [b, s, heads, 128] dense); k/v likewise
+    with kv_heads heads (kv_heads dividing heads: grouped K/V heads).
     cu_seqlens_*: int32 CUDA tensors [batch + 1] or None (dense).  Allocates
     ``out`` ([total_q, heads, 128] bf16) and ``lse`` ([heads, total_q] fp32)
     with torch when not given.  Raises FmhaError on a non-OK status.
@@ -124,8 +141,8 @@ def attention_forward(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_
     dense4 = q.dim() == 4
     if dense4:
         b, sq, h, d = q.shape
-        sk = k.shape[1]
-        qf, kf, vf = q.reshape(b * sq, h, d), k.reshape(b * sk, h, d), v.reshape(b * sk, h, d)
+        sk, hk = k.shape[1], k.shape[2]
+        qf, kf, vf = q.reshape(b * sq, h, d), k.reshape(b * sk, hk, d), v.reshape(b * sk, hk, d)
         batch, max_seqlen_q, max_seqlen_k = b, sq, sk
         if cu_seqlens_q is not None or cu_seqlens_k is not None:
             raise ValueError("4-D dense inputs take no cu_seqlens")
@@ -149,10 +166,10 @@ def attention_forward(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_
         out = torch.empty_like(qf)
     if lse is None and return_lse:
         lse = torch.empty((h, qf.shape[0]), dtype=torch.float32, device=qf.device)
-    st = fmha_fwd(qf, kf, vf, out, lse, cu_seqlens_q, cu_seqlens_k, batch, qf.shape[0], kf.shape[0],
-                  max_seqlen_q, max_seqlen_k, h, d, scale, int(bool(causal)), stream)
+    st = fmha_fwd_gqa(qf, kf, vf, out, lse, cu_seqlens_q, cu_seqlens_k, batch, qf.shape[0], kf.shape[0],
+                      max_seqlen_q, max_seqlen_k, h, kf.shape[1], d, scale, int(bool(causal)), stream)
     if st != FMHA_OK:
-        raise FmhaError(st, "fmha_fwd")
+        raise FmhaError(st, "fmha_fwd_gqa")
     if dense4:
         out = out.view(q.shape)
     return (out, lse) if return_lse else out

@@ -64,12 +64,13 @@ int configure_kernel() {
 
 }  // namespace
 
-extern "C" int fmha_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
-                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
-                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int heads,
-                        int head_dim, float scale, int causal, fmha_stream_t stream) {
+extern "C" int fmha_fwd_gqa(const void* q, const void* k, const void* v, void* out, float* lse,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
+                            int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int heads,
+                            int kv_heads, int head_dim, float scale, int causal, fmha_stream_t stream) {
   // ---- validation: no GPU work before this point
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return FMHA_ERR_INVALID_ARG;
+  if (heads < 1 || kv_heads < 1 || heads % kv_heads != 0) return FMHA_ERR_INVALID_ARG;
   if ((cu_seqlens_q == nullptr) != (cu_seqlens_k == nullptr)) return FMHA_ERR_INVALID_ARG;
   if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || heads < 1)
     return FMHA_ERR_INVALID_ARG;
@@ -94,9 +95,10 @@ extern "C" int fmha_fwd(const void* q, const void* k, const void* v, void* out, 
   fmha::FwdParams p;
   // a k/v tensor with no rows still needs a valid map extent; it is never read then
   const int tk = total_k > 0 ? total_k : 1;
-  if (!make_map(&p.tmap_q, q, total_q, heads) || !make_map(&p.tmap_k, k, tk, heads) ||
-      !make_map(&p.tmap_v, v, tk, heads))
+  if (!make_map(&p.tmap_q, q, total_q, heads) || !make_map(&p.tmap_k, k, tk, kv_heads) ||
+      !make_map(&p.tmap_v, v, tk, kv_heads))
     return FMHA_ERR_CUDA;
+  p.kv_group = heads / kv_heads;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.cu_q = cu_seqlens_q;
@@ -115,6 +117,14 @@ extern "C" int fmha_fwd(const void* q, const void* k, const void* v, void* out, 
   dim3 grid(static_cast<unsigned>(heads), static_cast<unsigned>(pairs), static_cast<unsigned>(batch));
   fmha::fmha_fwd_kernel<<<grid, fmha::kThreads, fmha::kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
+}
+
+extern "C" int fmha_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
+                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int heads,
+                        int head_dim, float scale, int causal, fmha_stream_t stream) {
+  return fmha_fwd_gqa(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, max_seqlen_q,
+                      max_seqlen_k, heads, heads, head_dim, scale, causal, stream);
 }
 
 extern "C" int fmha_get_device_status(fmha_stream_t stream, int* detail) {
@@ -142,7 +152,7 @@ extern "C" const char* fmha_status_string(int status) {
   }
 }
 
-extern "C" int fmha_version(void) { return 100; }
+extern "C" int fmha_version(void) { return 10100; }
 
 #ifdef FMHA_TRACE
 // Trace builds only: point the kernel's trace at a device buffer of

@@ -131,6 +131,7 @@ struct alignas(64) FwdParams {
   const int32_t* cu_k;
   int batch, total_q, total_k, max_seqlen_q, max_seqlen_k, heads;
   int causal;
+  int kv_group;             // query heads per K/V head (heads / kv_heads)
   float scale_log2;         // scale * log2(e)
   float rescale_threshold;  // skip the O rescale while the max grew by <= this (log2 units)
 };
@@ -379,7 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
 
   // TMA producer steps (one thread): the Q tiles, and ring load idx = K (even) or
   // V (odd) of key block idx / 2 into slot idx % kStages.
-  const int xh = h * kHeadDim;
+  const int xh = h * kHeadDim;                    // this head's columns in q / out
+  const int xkv = (h / p.kv_group) * kHeadDim;    // its K/V head's columns in k / v
   auto load_q = [&](int t, uint64_t pol) {
     if (n_blk(t) > 0) {
       const uint32_t bar = ctx.bar(kBarQFull + t);
@@ -397,8 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     const uint32_t dst = base + kOffKV + slot * kTileBytes;
     const CUtensorMap* m = (idx & 1) ? &p.tmap_v : &p.tmap_k;
     const int y = k0 + kBlockN * (idx >> 1);
-    ptx::tma_load_2d(dst, m, bar, xh, y, pol);
-    ptx::tma_load_2d(dst + kHalfBytes, m, bar, xh + 64, y, pol);
+    ptx::tma_load_2d(dst, m, bar, xkv, y, pol);
+    ptx::tma_load_2d(dst + kHalfBytes, m, bar, xkv + 64, y, pol);
   };
   // ring loads issued before the CTA-wide set-up sync (the ring starts empty)
   const int early_loads = min(kStages, 2 * n_kv);

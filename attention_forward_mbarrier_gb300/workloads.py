@@ -135,6 +135,12 @@ C5 = varlen("causal_t32768_h16_docs1", linspace_docs(32768, 1), 16,
 
 CONFIGS = {w.name: w for w in (C1, C2, C3, C4, C5)}
 
+# Grouped K/V heads on the varlen causal 8192-token shape: 32 query heads on 8
+# K/V heads (not one of the five named workloads; measured as an extension).
+GQA_C3 = varlen("gqa_varlen_causal_t8192_h32_kv8_docs4", linspace_docs(8192, 4), 32, kv_heads=8,
+                description="Varlen causal, 8192 packed tokens, 32 query heads on 8 K/V heads, 4 docs")
+EXTRA = {GQA_C3.name: GQA_C3}
+
 
 @dataclass
 class Inputs:

@@ -84,6 +84,23 @@ int fmha_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
              float scale, int causal, fmha_stream_t stream);
 
 /*
+ * fmha_fwd_gqa -- fmha_fwd with grouped K/V heads (grouped-query attention;
+ * kv_heads == 1 is multi-query attention).  Not on the pages above; the
+ * plainest extension of their operation: query head h attends with K/V head
+ * h / (heads / kv_heads), so consecutive query heads share one K/V head.
+ *
+ * k, v         bf16 [total_k, kv_heads, head_dim], contiguous, 16-byte aligned.
+ * kv_heads     >= 1 and a divisor of heads (else FMHA_ERR_INVALID_ARG).
+ * Every other argument, the return values and the error behaviour are those
+ * of fmha_fwd, which is fmha_fwd_gqa with kv_heads == heads.
+ */
+int fmha_fwd_gqa(const void *q, const void *k, const void *v, void *out, float *lse,
+                 const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                 int batch, int total_q, int total_k,
+                 int max_seqlen_q, int max_seqlen_k, int heads, int kv_heads, int head_dim,
+                 float scale, int causal, fmha_stream_t stream);
+
+/*
  * fmha_get_device_status -- synchronise `stream`, then read and clear the
  * device status word of the current device.  Returns FMHA_OK if no kernel
  * reported a problem since the last call, FMHA_ERR_TIMEOUT if a pipeline wait

@@ -35,7 +35,7 @@ def test_status_strings(lib):
     assert binding.status_string(0) == "ok"
     assert "timed out" in binding.status_string(binding.FMHA_ERR_TIMEOUT)
     assert binding.status_string(99) == "unknown status"
-    assert binding.fmha_version() >= 100
+    assert binding.fmha_version() >= 10100
 
 
 GOOD = dict(q=0x1000, k=0x2000, v=0x3000, out=0x4000, lse=0x5000, cu_seqlens_q=0x6000,
@@ -64,6 +64,24 @@ def test_invalid_arguments_rejected_on_host(lib, change, expected):
     args = dict(GOOD)
     args.update(change)
     assert binding.fmha_fwd(**args) == expected
+
+
+@pytest.mark.parametrize("kv_heads,expected", [
+    (0, binding.FMHA_ERR_INVALID_ARG),
+    (3, binding.FMHA_ERR_INVALID_ARG),   # does not divide heads = 4
+    (-2, binding.FMHA_ERR_INVALID_ARG),
+    (8, binding.FMHA_ERR_INVALID_ARG),   # more K/V heads than query heads
+])
+def test_invalid_kv_heads_rejected_on_host(lib, kv_heads, expected):
+    args = dict(GOOD)
+    args.update(kv_heads=kv_heads)
+    assert binding.fmha_fwd_gqa(**args) == expected
+
+
+def test_grouped_call_with_bad_common_argument_matches_fmha_fwd(lib):
+    args = dict(GOOD)
+    args.update(kv_heads=2, scale=float("nan"))
+    assert binding.fmha_fwd_gqa(**args) == binding.FMHA_ERR_INVALID_ARG
 
 
 def test_empty_problem_is_ok_without_gpu(lib):

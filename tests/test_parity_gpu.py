@@ -44,9 +44,14 @@ def run_gpu(inp, with_lse=True, canary=None):
     ck = None if inp.cu_seqlens_k is None else inp.cu_seqlens_k.to(dev)
     out = torch.empty_like(q) if canary is None else torch.full_like(q, canary)
     lse = torch.full((w.heads, w.total_q), 12345.0, dtype=torch.float32, device=dev) if with_lse else None
-    st = binding.fmha_fwd(q, k, v, out, lse, cq, ck, w.batch, w.total_q, w.total_k, w.max_seqlen_q,
-                          w.max_seqlen_k, w.heads, w.head_dim, w.softmax_scale, int(w.causal),
-                          torch.cuda.current_stream())
+    if w.kv_heads is None:
+        st = binding.fmha_fwd(q, k, v, out, lse, cq, ck, w.batch, w.total_q, w.total_k, w.max_seqlen_q,
+                              w.max_seqlen_k, w.heads, w.head_dim, w.softmax_scale, int(w.causal),
+                              torch.cuda.current_stream())
+    else:
+        st = binding.fmha_fwd_gqa(q, k, v, out, lse, cq, ck, w.batch, w.total_q, w.total_k, w.max_seqlen_q,
+                                  w.max_seqlen_k, w.heads, w.n_kv_heads, w.head_dim, w.softmax_scale,
+                                  int(w.causal), torch.cuda.current_stream())
     assert st == binding.FMHA_OK, binding.status_string(st)
     torch.cuda.synchronize()
     return out, lse
@@ -127,6 +132,36 @@ def test_uniform_inputs_wide_scores():
     # larger scale -> sharper softmax, exercises the lazy rescale path
     w = wl.varlen("sharp", (700, 300), 2, causal=True, scale=0.5)
     check_full(wl.make_inputs(w, seed=5))
+
+
+# ---------------------------------------------------------------- grouped K/V heads
+GQA = [
+    wl.varlen("gqa_causal_h8_kv2", (1, 129, 300, 513), 8, causal=True, kv_heads=2),
+    wl.varlen("mqa_noncausal_h6_kv1", (200, 77), 6, causal=False, seqlens_k=(260, 31), kv_heads=1),
+    wl.dense("gqa_dense_b2_h4_kv4_s300", 2, 300, 4, causal=False, kv_heads=4),
+    wl.dense("gqa_dense_b1_h16_kv2_s1000", 1, 1000, 16, causal=True, kv_heads=2),
+]
+
+
+@pytest.mark.parametrize("w", GQA, ids=lambda w: w.name)
+def test_grouped_kv_heads(w):
+    check_full(wl.make_inputs(w, seed=13))
+
+
+def test_grouped_equals_repeated_kv_bitwise():
+    # grouped K/V heads read exactly the bytes of the repeated multi-head call
+    w = wl.varlen("gqa_rep", (300, 129), 8, causal=True, kv_heads=2)
+    inp = wl.make_inputs(w, seed=14)
+    out, lse = run_gpu(inp)
+    wm = wl.varlen("gqa_rep_mha", (300, 129), 8, causal=True)
+    im = wl.Inputs(wm, inp.q, inp.k.repeat_interleave(4, dim=1).contiguous(),
+                   inp.v.repeat_interleave(4, dim=1).contiguous(), inp.cu_seqlens_q, inp.cu_seqlens_k)
+    out2, lse2 = run_gpu(im)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_gqa_workload_sampled():
+    check_sampled(wl.make_inputs(wl.GQA_C3, seed=0))
 
 
 # ---------------------------------------------------------------- properties
