@@ -603,10 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         int issued = early_loads;
         for (int idx = early_loads; idx < 2 * n_kv; ++idx) {
           // the slot's previous block (load idx - 4) was last read by the MMAs
-          // of step commit n: K_s by QK^T(s) (commit s), V_s by PV(s) (commit s + 1)
+          // of step commit n: K_s by QK^T(s) (commit s), V_s by PV(s) (commit s + 1);
+          // the first kStages loads find their slots empty
           const int prev = idx - kStages;
           const int n = (prev >> 1) + (prev & 1);
-          if (!wait_bar(ctx, kBarStepDone + (n & 1), (n >> 1) & 1, kRoleLoad)) break;
+          if (prev >= 0 && !wait_bar(ctx, kBarStepDone + (n & 1), (n >> 1) & 1, kRoleLoad)) break;
           if (idx < 400) FMHA_TRACE_AT(kTrLoad + idx);
           load_kv(idx, pol_kv);
           ++issued;
@@ -631,16 +632,17 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         const uint64_t kv_desc_mn = desc_mnmajor(base + kOffKV);
         bool issued_any = false;
         bool ok = true;
-#pragma unroll
-        for (int t = 0; t < kTiles; ++t)
-          if (ok && n_blk(t) > 0) ok = wait_bar(ctx, kBarQFull + t, 0, kRoleMma);
-        if (ok && n_kv > 0) ok = wait_bar(ctx, kBarKVFull + 0, 0, kRoleMma);
+        if (n_kv > 0) ok = wait_bar(ctx, kBarKVFull + 0, 0, kRoleMma);
         if (ok && n_kv > 0) {
-          ptx::tc_fence_after();
+          // each tile's first QK^T as soon as its own Q tile has landed
 #pragma unroll
           for (int t = 0; t < kTiles; ++t) {
-            if (n_blk(t) > 0) {
+            if (ok && n_blk(t) > 0) {
+              ok = wait_bar(ctx, kBarQFull + t, 0, kRoleMma);
+              if (!ok) break;
+              ptx::tc_fence_after();
               issue_qk(tmem + col_s(t), q_desc[t], kv_desc);
+              issued_any = true;
               if (t != t_last) ptx::mma_commit(ctx.bar(kBarSFull0));
             }
           }
@@ -650,7 +652,6 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           // test build only: step commit 0 is never made, so the waits on it
           // expire and the kernel must report a timeout and shut down cleanly
 #endif
-          issued_any = true;
           for (int j = 0; j < n_kv && ok; ++j) {
             const int vidx = 2 * j + 1, vslot = vidx % kStages;
             if (!wait_bar(ctx, kBarKVFull + vslot, (vidx / kStages) & 1, kRoleMma)) break;
