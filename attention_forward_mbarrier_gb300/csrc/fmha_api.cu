@@ -1,8 +1,8 @@
 // fmha_api.cu -- host launcher and C ABI of libfmha.so (declared in fmha.h).
 //
 // Validates arguments without touching the GPU, encodes the three TMA tensor
-// maps (Q, K, V viewed as 2-D [tokens, heads * 128] bf16, 64 x 128 boxes with
-// 128-byte swizzle), and launches one CTA per (head, 256-row query block,
+// maps (Q, K, V viewed as 2-D [tokens, heads * head_dim] bf16, 64 x 128 boxes
+// with 128-byte swizzle), and launches the kernel for head_dim 64 or 128 one CTA per (head, 256-row query block,
 // sequence).  Causal launches walk query blocks from the last to the first so
 // the longest units start first.
 #include <cuda.h>
@@ -32,12 +32,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [tokens, heads * 128] bf16, row stride heads * 256 bytes, box 64 x 128, 128B swizzle.
-bool make_map(CUtensorMap* m, const void* ptr, int tokens, int heads) {
+// [tokens, heads * head_dim] bf16, row stride heads * head_dim * 2 bytes, box 64 x 128,
+// 128B swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int tokens, int heads, int head_dim) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads) * fmha::kHeadDim, static_cast<cuuint64_t>(tokens)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads) * fmha::kHeadDim * 2};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads) * head_dim, static_cast<cuuint64_t>(tokens)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads) * head_dim * 2};
   cuuint32_t box[2] = {64, 128};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
@@ -48,18 +49,27 @@ bool make_map(CUtensorMap* m, const void* ptr, int tokens, int heads) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+template <int HD>
 int configure_kernel() {
   static int rc = -1;
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   // per-process attribute; re-applied cheaply if a previous attempt failed
   if (rc != 0) {
-    rc = cudaFuncSetAttribute(fmha::fmha_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(fmha::kSmemBytes)) == cudaSuccess
+    rc = cudaFuncSetAttribute(fmha::fmha_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(fmha::Dims<HD>::kSmemBytes)) == cudaSuccess
              ? 0
              : 1;
   }
   return rc;
+}
+
+template <int HD>
+int launch(const fmha::FwdParams& p, dim3 grid, fmha_stream_t stream) {
+  if (configure_kernel<HD>() != 0) return FMHA_ERR_CUDA;
+  fmha::fmha_fwd_kernel<HD><<<grid, fmha::kThreads, fmha::Dims<HD>::kSmemBytes,
+                              reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
 }
 
 }  // namespace
@@ -84,9 +94,9 @@ extern "C" int fmha_fwd_gqa(const void* q, const void* k, const void* v, void* o
         static_cast<int64_t>(batch) * max_seqlen_k != total_k)
       return FMHA_ERR_INVALID_ARG;
   }
-  if (head_dim != fmha::kHeadDim) return FMHA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return FMHA_ERR_UNSUPPORTED;
   if (batch > 65535) return FMHA_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(heads) * fmha::kHeadDim * 2 >= (int64_t(1) << 32)) return FMHA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(heads) * head_dim * 2 >= (int64_t(1) << 32)) return FMHA_ERR_UNSUPPORTED;
 
   const int pairs = (max_seqlen_q + fmha::kTiles * fmha::kBlockM - 1) / (fmha::kTiles * fmha::kBlockM);
   if (batch == 0 || total_q == 0 || pairs == 0) return FMHA_OK;  // nothing to compute
@@ -95,8 +105,8 @@ extern "C" int fmha_fwd_gqa(const void* q, const void* k, const void* v, void* o
   fmha::FwdParams p;
   // a k/v tensor with no rows still needs a valid map extent; it is never read then
   const int tk = total_k > 0 ? total_k : 1;
-  if (!make_map(&p.tmap_q, q, total_q, heads) || !make_map(&p.tmap_k, k, tk, kv_heads) ||
-      !make_map(&p.tmap_v, v, tk, kv_heads))
+  if (!make_map(&p.tmap_q, q, total_q, heads, head_dim) || !make_map(&p.tmap_k, k, tk, kv_heads, head_dim) ||
+      !make_map(&p.tmap_v, v, tk, kv_heads, head_dim))
     return FMHA_ERR_CUDA;
   p.kv_group = heads / kv_heads;
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -113,10 +123,8 @@ extern "C" int fmha_fwd_gqa(const void* q, const void* k, const void* v, void* o
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.rescale_threshold = 8.0f;
 
-  if (configure_kernel() != 0) return FMHA_ERR_CUDA;
   dim3 grid(static_cast<unsigned>(heads), static_cast<unsigned>(pairs), static_cast<unsigned>(batch));
-  fmha::fmha_fwd_kernel<<<grid, fmha::kThreads, fmha::kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-  return cudaGetLastError() == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
+  return head_dim == 64 ? launch<64>(p, grid, stream) : launch<128>(p, grid, stream);
 }
 
 extern "C" int fmha_fwd(const void* q, const void* k, const void* v, void* out, float* lse,

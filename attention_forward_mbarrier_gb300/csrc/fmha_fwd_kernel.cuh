@@ -1,7 +1,8 @@
 // fmha_fwd_kernel.cuh -- fused attention forward for sm_103a.
 //
 // O = softmax(scale * Q K^T [+ causal mask]) V and the per-row log-sum-exp, for
-// bf16 [tokens, heads, 128] tensors, dense or varlen (cu_seqlens), after
+// bf16 [tokens, heads, head_dim] tensors (head_dim 128 or 64), dense or varlen
+// (cu_seqlens), after
 // "[BUG] Unexpected Slower Performance in C++ CuTe (77_blackwell_fmha) vs
 // Python CuTe DSL (fmha.py) on Jetson Thor" (sections "Test Commands" and
 // "Implementation Differences in softmax_step") and "[BUG] CuTe DSL 4.7/4.8
@@ -25,7 +26,8 @@
 //                   signalled with tcgen05.commit on mbarriers;
 //   warps 14, 15    idle (barrier observers in the trace build).
 // Tensor memory (512 columns): S0/P0 [0,128), S1/P1 [128,256), O0 [256,384),
-// O1 [384,512).  P (bf16 pairs) overwrites the first 64 columns of its S.
+// O1 [384,512) (head_dim 64 uses the first 64 columns of each O).  P (bf16
+// pairs) overwrites the first 64 columns of its S.
 //
 // Every mbarrier wait is bounded in time: on expiry the kernel records an
 // error word, raises a CTA-wide abort flag, lets in-flight copies and MMAs
@@ -40,7 +42,6 @@
 
 namespace fmha {
 
-constexpr int kHeadDim = 128;
 constexpr int kBlockM = 128;   // query rows per tile (MMA M)
 constexpr int kBlockN = 128;   // keys per block (MMA N of QK^T, K of PV)
 constexpr int kTiles = 2;      // query tiles per CTA
@@ -48,20 +49,30 @@ constexpr int kTiles = 2;      // query tiles per CTA
 // flight).  The slot-release protocol below relies on exactly four.
 constexpr int kStages = 4;
 constexpr int kThreads = 512;
-constexpr uint32_t kTileBytes = kBlockM * kHeadDim * 2;  // 32 KiB bf16 tile
-constexpr uint32_t kHalfBytes = kTileBytes / 2;          // 64 columns x 128 rows
+// A tile (128 rows: queries, keys or values) is stored as 64-column halves
+// of 128 rows x 128 bytes (16 KiB, 128-byte swizzle): one half for head_dim
+// 64, two for head_dim 128.
+constexpr uint32_t kHalfBytes = kBlockM * 64 * 2;
 constexpr uint32_t kTmemCols = 512;
-
-// shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = kOffQ + kTiles * kTileBytes;
-constexpr uint32_t kOffBar = kOffKV + kStages * kTileBytes;
 constexpr uint32_t kNumBars = 14;
-constexpr uint32_t kOffMisc = kOffBar + 256;   // tmem base slot, abort flag
-constexpr uint32_t kSmemUsed = kOffBar + 512;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kNumBars * 8 <= 256, "barrier area");
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+// Sizes that depend on the head dimension (64 or 128).  Shared memory map,
+// offsets from a 1024-byte aligned base: Q tiles, the K/V ring, barriers,
+// misc words.
+template <int HD>
+struct Dims {
+  static_assert(HD == 64 || HD == 128, "head_dim");
+  static constexpr int kHeadDim = HD;
+  static constexpr int kHalves = HD / 64;
+  static constexpr uint32_t kTileBytes = kBlockM * HD * 2;  // one Q tile / K or V block
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffKV = kOffQ + kTiles * kTileBytes;
+  static constexpr uint32_t kOffBar = kOffKV + kStages * kTileBytes;
+  static constexpr uint32_t kOffMisc = kOffBar + 256;  // tmem base slot, abort flag
+  static constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
 
 // Barrier ids.  Every tcgen05.commit stalls the tensor pipe for ~70-140
 // cycles (measured), so the MMA warp commits twice per KV step: S ready for
@@ -237,16 +248,16 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr) {
 }
 // A descriptor's start address is its low 14 bits in 16-byte units; every
 // offset below stays inside the 256 KiB window, so offsets add without carry.
-constexpr uint64_t kSlotDescStep = kTileBytes >> 4;
 
 // Each MMA is one instruction with a base descriptor plus an immediate offset:
 // a single issuing thread then keeps the tensor core fed (M128 N128 K16 every
 // 64 cycles, measured).
+template <int HD>
 __device__ __forceinline__ void issue_qk(uint32_t tmem_d, uint64_t q_desc, uint64_t k_desc) {
   constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, kBlockN, false, false);
   ptx::mma_ss_imm<false>(tmem_d, q_desc, k_desc, idesc);
 #pragma unroll
-  for (int k = 1; k < kHeadDim / 16; ++k) {
+  for (int k = 1; k < HD / 16; ++k) {
     const uint64_t off = ((k >> 2) * kHalfBytes + (k & 3) * 32u) >> 4;
     ptx::mma_ss_imm<true>(tmem_d, q_desc + off, k_desc + off, idesc);
   }
@@ -257,8 +268,9 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_d, uint64_t q_desc, uint6
 // same swizzled layout as K: head dims contiguous within a 128-byte row, the
 // second 64 head dims 16 KiB further (leading offset), 8-key groups 1024
 // bytes apart (stride offset), 16 keys = 2048 bytes per step.
+template <int HD>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint64_t v_desc, bool accumulate) {
-  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, kHeadDim, false, true);
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, HD, false, true);
   if (accumulate)
     ptx::mma_ts_imm<true>(tmem_d, tmem_p, v_desc, idesc);
   else
@@ -312,7 +324,13 @@ __device__ __forceinline__ float exp_pass(const float (&s)[128], float c, float 
 }
 
 // ---------------------------------------------------------------------------
+template <int HD>
 __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using D = Dims<HD>;
+  constexpr int kHeadDim = HD;
+  constexpr uint32_t kTileBytes = D::kTileBytes;
+  constexpr uint32_t kOffQ = D::kOffQ, kOffKV = D::kOffKV, kOffBar = D::kOffBar, kOffMisc = D::kOffMisc;
+  constexpr uint64_t kSlotDescStep = kTileBytes >> 4;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -389,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       const uint32_t dst = base + kOffQ + t * kTileBytes;
       const int y = q0 + m0 + kBlockM * t;
       ptx::tma_load_2d(dst, &p.tmap_q, bar, xh, y, pol);
-      ptx::tma_load_2d(dst + kHalfBytes, &p.tmap_q, bar, xh + 64, y, pol);
+      if (D::kHalves == 2) ptx::tma_load_2d(dst + kHalfBytes, &p.tmap_q, bar, xh + 64, y, pol);
     }
   };
   auto load_kv = [&](int idx, uint64_t pol) {
@@ -400,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     const CUtensorMap* m = (idx & 1) ? &p.tmap_v : &p.tmap_k;
     const int y = k0 + kBlockN * (idx >> 1);
     ptx::tma_load_2d(dst, m, bar, xkv, y, pol);
-    ptx::tma_load_2d(dst + kHalfBytes, m, bar, xkv + 64, y, pol);
+    if (D::kHalves == 2) ptx::tma_load_2d(dst + kHalfBytes, m, bar, xkv + 64, y, pol);
   };
   // ring loads issued before the CTA-wide set-up sync (the ring starts empty)
   const int early_loads = min(kStages, 2 * n_kv);
@@ -492,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         // committed after it) and PV_t(j) waits for this warp's P hand-off.
         const uint32_t t_o = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16) + col_o(t);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < HD / 32; ++cc) {
           float o[32];
           ptx::tmem_ld32_wait(t_o + 32u * cc, o);
           uint32_t u[32];
@@ -534,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         const uint32_t tile_smem = base + kOffQ + static_cast<uint32_t>(t) * kTileBytes;
         const uint32_t row_addr = tile_smem + static_cast<uint32_t>(r) * 128u;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < HD / 32; ++cc) {
           float o[32];
           ptx::tmem_ld32_wait(t_o + 32u * cc, o);
           const uint32_t half_addr = row_addr + static_cast<uint32_t>(cc >> 1) * kHalfBytes;
@@ -550,13 +568,14 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         }
         if (r == 0) FMHA_TRACE_AT(kTrEpilogue + 4 * t + 2);
         __syncwarp();
-        // lanes 0-15: row 2i of the warp, lanes 16-31: row 2i + 1; lane & 15
-        // picks the 16-byte chunk (8 head dims) of the 256-byte row
-        const int k16 = lane & 15;
-        const uint32_t hf = static_cast<uint32_t>(k16 >> 3), c = static_cast<uint32_t>(k16 & 7);
+        // HD / 8 lanes per row, each one 16-byte chunk (8 head dims): every
+        // store instruction of the warp covers 32 / (HD / 8) complete rows
+        constexpr int kLanesPerRow = HD / 8, kRowsPerInst = 32 / kLanesPerRow;
+        const int kc = lane % kLanesPerRow;
+        const uint32_t hf = static_cast<uint32_t>(kc >> 3), c = static_cast<uint32_t>(kc & 7);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int rt = 32 * (warp & 3) + 2 * i + (lane >> 4);  // row within the tile
+        for (int i = 0; i < 32 / kRowsPerInst; ++i) {
+          const int rt = 32 * (warp & 3) + kRowsPerInst * i + lane / kLanesPerRow;  // row within the tile
           const uint4 v = ptx::ld_shared_v4(tile_smem + hf * kHalfBytes + static_cast<uint32_t>(rt) * 128u +
                                             ((c ^ static_cast<uint32_t>(rt & 7)) << 4));
           __nv_bfloat16* dst =
@@ -567,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         __nv_bfloat16* dst =
             p.out + (static_cast<size_t>(q0 + row) * p.heads + h) * static_cast<size_t>(kHeadDim);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < HD / 32; ++cc) {
           float o[32];
           if (nb > 0) {
             ptx::tmem_ld32_wait(t_o + 32u * cc, o);
@@ -641,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
               ok = wait_bar(ctx, kBarQFull + t, 0, kRoleMma);
               if (!ok) break;
               ptx::tc_fence_after();
-              issue_qk(tmem + col_s(t), q_desc[t], kv_desc);
+              issue_qk<HD>(tmem + col_s(t), q_desc[t], kv_desc);
               issued_any = true;
               if (t != t_last) ptx::mma_commit(ctx.bar(kBarSFull0));
             }
@@ -669,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
               }
               if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 1 + 2 * t);
               ptx::tc_fence_after();
-              issue_pv(tmem + col_o(t), tmem + col_s(t), kv_desc_mn + kSlotDescStep * vslot, j > 0);
+              issue_pv<HD>(tmem + col_o(t), tmem + col_s(t), kv_desc_mn + kSlotDescStep * vslot, j > 0);
               if (j + 1 < n_blk(t)) {
                 if (!k_ready) {
                   if (!wait_bar(ctx, kBarKVFull + kslot, (kidx / kStages) & 1, kRoleMma)) {
@@ -680,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
                   k_ready = true;
                 }
                 if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 6 + t);
-                issue_qk(tmem + col_s(t), q_desc[t], kv_desc + kSlotDescStep * kslot);
+                issue_qk<HD>(tmem + col_s(t), q_desc[t], kv_desc + kSlotDescStep * kslot);
                 if (t != t_last) ptx::mma_commit(ctx.bar(kBarSFull0));
               } else {
                 ptx::mma_commit(ctx.bar(kBarOFinal + t));

@@ -139,7 +139,10 @@ CONFIGS = {w.name: w for w in (C1, C2, C3, C4, C5)}
 # K/V heads (not one of the five named workloads; measured as an extension).
 GQA_C3 = varlen("gqa_varlen_causal_t8192_h32_kv8_docs4", linspace_docs(8192, 4), 32, kv_heads=8,
                 description="Varlen causal, 8192 packed tokens, 32 query heads on 8 K/V heads, 4 docs")
-EXTRA = {GQA_C3.name: GQA_C3}
+# head_dim 64 on the single-document causal 32768-token shape with 32 heads
+D64_C5 = varlen("d64_causal_t32768_h32_docs1", linspace_docs(32768, 1), 32, head_dim=64,
+                description="Single-document causal, 32768 tokens, 32 heads, head_dim 64")
+EXTRA = {GQA_C3.name: GQA_C3, D64_C5.name: D64_C5}
 
 
 @dataclass

@@ -476,7 +476,8 @@ def main():
     ap.add_argument("--flush", choices=["write+read", "write"], default="write+read",
                     help="L2 flush between timed steps (see L2Flusher)")
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--secondary", default=",".join([wl.C3.name, wl.C4.name, wl.C5.name, wl.GQA_C3.name]),
+    ap.add_argument("--secondary", default=",".join([wl.C3.name, wl.C4.name, wl.C5.name, wl.GQA_C3.name,
+                                                     wl.D64_C5.name]),
                     help="comma-separated workloads timed kernel-only after the main line")
     ap.add_argument("--clock-window", type=float, default=1.0,
                     help="seconds of back-to-back launches before the timed region")

@@ -38,7 +38,7 @@ typedef struct CUstream_st *fmha_stream_t;
 enum fmha_status_code {
     FMHA_OK = 0,
     FMHA_ERR_INVALID_ARG = 1, /* a null or misaligned pointer, inconsistent sizes */
-    FMHA_ERR_UNSUPPORTED = 2, /* a valid request this build does not handle (head_dim != 128) */
+    FMHA_ERR_UNSUPPORTED = 2, /* a valid request this build does not handle (head_dim not 64 or 128) */
     FMHA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, tensor map) */
     FMHA_ERR_TIMEOUT = 4      /* a device-side pipeline wait gave up (see fmha_get_device_status) */
 };
@@ -66,7 +66,8 @@ enum fmha_status_code {
  * max_seqlen_k the page's varlen call (the caller's responsibility; a longer
  *              sequence is not fully computed).
  * heads        >= 1.
- * head_dim     must be 128 (else FMHA_ERR_UNSUPPORTED).
+ * head_dim     64 or 128 (else FMHA_ERR_UNSUPPORTED).  The pages' runs use
+ *              128; 64 is the adjacent size their command line also takes.
  * scale        finite softmax scale, e.g. 1/sqrt(128); no default is applied.
  * causal       0 or 1.
  * stream       CUDA stream the kernel is enqueued on.

@@ -120,6 +120,11 @@ EDGE = [
     wl.dense("dense_b3_s300", 3, 300, 4, causal=False),
     wl.dense("dense_b2_causal_s513", 2, 513, 2, causal=True),
     wl.dense("dense_b1_h1_s2225", 1, 2225, 1, causal=False),
+    # decode-style: a few new query rows against a long key cache (the causal
+    # diagonal is bottom-right aligned, so every new row sees the whole cache
+    # up to its own position)
+    wl.varlen("decode_causal", (1, 4, 16), 4, causal=True, seqlens_k=(2000, 1031, 300)),
+    wl.dense("decode_dense_b3_q1_k777", 3, 1, 2, causal=False, seqlen_k=777),
 ]
 
 
@@ -132,6 +137,25 @@ def test_uniform_inputs_wide_scores():
     # larger scale -> sharper softmax, exercises the lazy rescale path
     w = wl.varlen("sharp", (700, 300), 2, causal=True, scale=0.5)
     check_full(wl.make_inputs(w, seed=5))
+
+
+# ---------------------------------------------------------------- head_dim 64
+D64 = [
+    wl.varlen("d64_ragged_causal", (1, 127, 128, 129, 255, 256, 257, 383), 2, head_dim=64, causal=True),
+    wl.varlen("d64_noncausal_lq_ne_lk", (70, 260), 3, head_dim=64, causal=False, seqlens_k=(500, 33)),
+    wl.dense("d64_dense_b2_h8_s1000", 2, 1000, 8, head_dim=64, causal=False),
+    wl.varlen("d64_gqa_causal_h8_kv2", (300, 513), 8, head_dim=64, causal=True, kv_heads=2),
+    wl.varlen("d64_sharp", (700, 300), 2, head_dim=64, causal=True, scale=0.5),
+]
+
+
+@pytest.mark.parametrize("w", D64, ids=lambda w: w.name)
+def test_head_dim_64(w):
+    check_full(wl.make_inputs(w, seed=17))
+
+
+def test_head_dim_64_workload_sampled():
+    check_sampled(wl.make_inputs(wl.D64_C5, seed=0))
 
 
 # ---------------------------------------------------------------- grouped K/V heads
