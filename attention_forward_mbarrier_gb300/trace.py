@@ -248,6 +248,7 @@ def main():
     stamps, ctas = run(w, flags=args.flags.split(), flush_l2=not args.no_flush)
     if args.raw:
         np.save(args.raw, stamps)
+        np.save(args.raw.replace(".npy", "") + "_ctas.npy", ctas)
     print(json.dumps({"workload": w.name, "flags": args.flags,
                       "cycles_per_kv_step_median": summarize(stamps[args.row]),
                       "cta_times": summarize_ctas(ctas),

@@ -139,6 +139,27 @@ def test_uniform_inputs_wide_scores():
     check_full(wl.make_inputs(w, seed=5))
 
 
+# ---------------------------------------------------------------- large index ranges
+def test_many_tiny_sequences_full():
+    # 3000 sequences of 0-5 tokens: a large grid.z, empty and one-row docs
+    rng = np.random.default_rng(21)
+    lens = tuple(int(x) for x in rng.integers(0, 6, size=3000))
+    w = wl.varlen("many_tiny", lens, 2, causal=True)
+    check_full(wl.make_inputs(w, seed=21))
+
+
+def test_long_sequence_sampled():
+    # 70000 tokens in one causal sequence: query and key rows beyond 2^16
+    w = wl.varlen("long_70000", (70000,), 2, causal=True)
+    check_sampled(wl.make_inputs(w, seed=22), n_random=96)
+
+
+def test_many_heads_sampled():
+    # 256 heads: wide rows (heads x 256 bytes) in the tensor maps
+    w = wl.dense("heads_256", 1, 700, 256, causal=False)
+    check_sampled(wl.make_inputs(w, seed=23), n_random=256)
+
+
 # ---------------------------------------------------------------- head_dim 64
 D64 = [
     wl.varlen("d64_ragged_causal", (1, 127, 128, 129, 255, 256, 257, 383), 2, head_dim=64, causal=True),
