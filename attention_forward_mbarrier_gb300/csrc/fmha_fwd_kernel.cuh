@@ -89,23 +89,13 @@ constexpr int kBarOFinal = 11;   // [2]  last PV of tile t complete
 constexpr int kBarMmaDone = 13;  //      every MMA retired
 static_assert(kBarMmaDone + 1 == static_cast<int>(kNumBars), "ids");
 
-// bf16 packing of P: cvt.rn (round to nearest even, default) or integer
-// round-half-up (-DFMHA_P_PACK_ALU=1)
-#if defined(FMHA_P_PACK_ALU) && FMHA_P_PACK_ALU
-#define FMHA_P_PACK ptx::pack_bf16x2_alu
-#else
-#define FMHA_P_PACK ptx::pack_bf16x2
-#endif
 
 // Warpgroup of each role.  Warp w reaches TMEM lanes 32 (w % 4) .. + 31, so
-// any warpgroup can hold a tile's softmax.  FMHA_CONTROL_FIRST=1 puts the
-// producer / MMA warpgroup at warps 0-3 instead of 12-15.
-#ifndef FMHA_CONTROL_FIRST
-#define FMHA_CONTROL_FIRST 0
-#endif
-constexpr int kWgControl = FMHA_CONTROL_FIRST ? 0 : 3;
-constexpr int kWgSoftmax0 = FMHA_CONTROL_FIRST ? 1 : 0;  // softmax of tile 0; tile 1 is the next warpgroup
-constexpr int kWgIdle = FMHA_CONTROL_FIRST ? 3 : 2;
+// any warpgroup could hold a tile's softmax (placing the control warpgroup
+// first measured the same).
+constexpr int kWgControl = 3;
+constexpr int kWgSoftmax0 = 0;  // softmax of tile 0; tile 1 is the next warpgroup
+constexpr int kWgIdle = 2;
 constexpr int kWarpProducer = 4 * kWgControl;      // TMA producer, barrier set-up
 constexpr int kWarpMma = 4 * kWgControl + 1;       // MMA issuer, TMEM owner
 
@@ -116,13 +106,6 @@ constexpr int kRoleSoftmax = 1, kRoleLoad = 3, kRoleMma = 4, kRoleDrain = 5;
 #define FMHA_WAIT_LIMIT_NS 1000000000ull
 #endif
 constexpr uint64_t kWaitLimitNs = FMHA_WAIT_LIMIT_NS;  // per wait (1 s by default)
-#ifndef FMHA_WAIT_HINT_NS
-#define FMHA_WAIT_HINT_NS 0
-#endif
-// A waiting thread sleeps inside mbarrier.try_wait for up to this long (it is
-// woken when the phase completes): polling warps would otherwise take issue
-// slots from the softmax warps on the same sub-partition.  0 = plain polling.
-constexpr uint32_t kWaitHintNs = FMHA_WAIT_HINT_NS;
 
 // Register budgets per warpgroup after the split (sum x 128 threads = 64K).
 // Helper calls in these regions must be inlined: ptxas cannot place an ABI
@@ -188,7 +171,7 @@ struct Ctx {
 __device__ __forceinline__ bool wait_slow(const Ctx& c, uint32_t bar, uint32_t parity, int code) {
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
-    if (kWaitHintNs ? ptx::mbar_try_wait_sleep(bar, parity, kWaitHintNs) : ptx::mbar_try_wait(bar, parity))
+    if (ptx::mbar_try_wait(bar, parity))
       return true;
     if (*c.abort_flag) return false;
     if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -215,7 +198,7 @@ __device__ __forceinline__ bool wait_bar_warp(const Ctx& c, int id, uint32_t par
 __device__ __forceinline__ void wait_drain(const Ctx& c, int id, uint32_t parity) {
   const uint32_t b = c.bar(id);
   const uint64_t t0 = ptx::globaltimer_ns();
-  while (!(kWaitHintNs ? ptx::mbar_try_wait_sleep(b, parity, kWaitHintNs) : ptx::mbar_try_wait(b, parity))) {
+  while (!ptx::mbar_try_wait(b, parity)) {
     if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
       atomicCAS(&g_status, 0, 1 + kRoleDrain * 256 + id);
       return;
@@ -313,7 +296,7 @@ __device__ __forceinline__ float exp_pass(const float (&s)[128], float c, float 
       const float p0 = ptx::ex2_approx(x.x);
       const float p1 = ptx::ex2_approx(x.y);
       acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
-      pk[i] = FMHA_P_PACK(p0, p1);
+      pk[i] = ptx::pack_bf16x2(p0, p1);
     }
     ptx::tmem_st32(t_s + 32u * half, pk);
   }

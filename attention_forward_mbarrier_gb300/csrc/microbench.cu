@@ -75,6 +75,11 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t h) {
   return make_float2(lo, hi);
 }
 
+// bf16x2 pack by integer rounding (round half up on the magnitude): the
+// alternative to cvt.rn.bf16x2.f32 that the exp-loop probe compares.
+__device__ __forceinline__ uint32_t pack_bf16x2_alu(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo) + 0x8000u, __float_as_uint(hi) + 0x8000u, 0x7632);
+}
 }  // namespace ptx_probe
 
 constexpr int kAluThreads = 512;
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(threads, 1) exp_loop_probe(int reps, long long
         }
         acc[i] = __fadd2_rn(acc[i], make_float2(p0, p1));
         if (variant == 4)
-          pk[i] = ptx::pack_bf16x2_alu(p0, p1);
+          pk[i] = ptx_probe::pack_bf16x2_alu(p0, p1);
         else
           pk[i] = ptx::pack_bf16x2(p0, p1);
       }

@@ -53,21 +53,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// As mbar_try_wait, but the thread may sleep up to `hint_ns` nanoseconds
-// inside the instruction (it resumes when the phase completes), so a waiting
-// warp does not spend issue slots polling.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -91,14 +76,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
-}
-
-// Warm L2 with one box of a tensor map (no shared memory, no completion signal).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(x), "r"(y)
-               : "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_last() {
@@ -332,15 +309,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
-}
-
-// Pack two non-negative finite floats to bf16x2 with integer ops only (lo in
-// bits 0..15): add half a bf16 ulp to each bit pattern and keep the high
-// halves.  This rounds half up, which differs from round-to-nearest-even only
-// when the low 16 bits are exactly 0x8000, and keeps the conversion off the
-// unit that executes ex2.
-__device__ __forceinline__ uint32_t pack_bf16x2_alu(float lo, float hi) {
-  return __byte_perm(__float_as_uint(lo) + 0x8000u, __float_as_uint(hi) + 0x8000u, 0x7632);
 }
 
 // Pack two floats to bf16x2 (round to nearest even): lo in bits 0..15.
