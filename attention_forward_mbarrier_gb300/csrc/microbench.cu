@@ -543,24 +543,7 @@ bool alloc(long long** d_out, int** d_status, int n_ctas) {
   return cudaMemset(*d_status, 0, 2 * sizeof(int)) == cudaSuccess;
 }
 
-__global__ void smem_touch_kernel(int* sink) {
-  extern __shared__ int sm[];
-  if (threadIdx.x == 0 && sink == nullptr) sm[0] = 1;  // never true; keeps the allocation
-}
-
 }  // namespace
-
-// Launch an empty kernel that requests `smem_bytes` of dynamic shared memory
-// per CTA on n_ctas CTAs (no synchronisation).  Used to see what a shared
-// memory carve-out change costs the next kernel.  Returns 0 or 2.
-extern "C" int fmha_microbench_smem_touch(int smem_bytes, int n_ctas, void* stream) {
-  if (cudaFuncSetAttribute(smem_touch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
-    return 2;
-  int one = 1;
-  int* dummy = reinterpret_cast<int*>(&one);
-  smem_touch_kernel<<<n_ctas, 128, smem_bytes, static_cast<cudaStream_t>(stream)>>>(dummy);
-  return cudaGetLastError() == cudaSuccess ? 0 : 2;
-}
 
 extern "C" int fmha_microbench_alu(int which, int reps, long long* out_cycles, int n_ctas) {
   if (which < 0 || which > 4 || reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
