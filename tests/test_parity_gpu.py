@@ -209,6 +209,44 @@ def test_gqa_workload_sampled():
     check_sampled(wl.make_inputs(wl.GQA_C3, seed=0))
 
 
+# ---------------------------------------------------------------- CUDA graphs
+def test_cuda_graph_capture_and_replay():
+    # The call does no host synchronisation or allocation and reads its inputs
+    # through the pointers it was given, so it can be captured in a CUDA graph;
+    # a replay after the inputs were overwritten in place computes on the new values.
+    w = wl.varlen("graph", (300, 129, 700), 4, causal=True)
+    first, second = wl.make_inputs(w, seed=30), wl.make_inputs(w, seed=31)
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in (first.q, first.k, first.v))
+    cu = first.cu_seqlens_q.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.heads, w.total_q), dtype=torch.float32, device=dev)
+
+    def call(stream):
+        return binding.fmha_fwd(q, k, v, out, lse, cu, cu, w.batch, w.total_q, w.total_k, w.max_seqlen_q,
+                                w.max_seqlen_k, w.heads, w.head_dim, w.softmax_scale, 1, stream)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # first call outside the capture (per-process kernel set-up)
+        assert call(side) == binding.FMHA_OK
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        assert call(torch.cuda.current_stream()) == binding.FMHA_OK
+    for inp in (first, second):
+        q.copy_(inp.q.to(dev))
+        k.copy_(inp.k.to(dev))
+        v.copy_(inp.v.to(dev))
+        out.zero_()
+        lse.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        ref_o, ref_l = oracle.oracle_fwd(*inp.oracle_args())
+        compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
+
+
 # ---------------------------------------------------------------- properties
 def test_causal_row0_equals_v0():
     # row 0 of every sequence sees only key 0: p = 1, l = 1, O_0 = V_0 exactly
