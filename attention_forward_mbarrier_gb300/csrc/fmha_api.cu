@@ -3,8 +3,9 @@
 // Validates arguments without touching the GPU, encodes the three TMA tensor
 // maps (Q, K, V viewed as 2-D [tokens, heads * head_dim] bf16, 64 x 128 boxes
 // with 128-byte swizzle), and launches the kernel for head_dim 64 or 128 one CTA per (head, 256-row query block,
-// sequence).  Causal launches walk query blocks from the last to the first so
-// the longest units start first.
+// sequence).  The kernel orders the units in groups of a few heads, and causal
+// launches walk query blocks from the last to the first so the longest units
+// start first.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -46,6 +47,12 @@ bool make_map(CUtensorMap* m, const void* ptr, int tokens, int heads, int head_d
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+// Head-group rasterisation: heads per group, and the per-sequence K/V size
+// above which it is used (a little under the 129 MB L2, which also holds the
+// Q and O streams).
+constexpr int kHeadGroup = 4;
+constexpr int64_t kL2GroupBytes = int64_t(96) << 20;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -100,7 +107,12 @@ extern "C" int fmha_fwd_gqa(const void* q, const void* k, const void* v, void* o
 
   const int pairs = (max_seqlen_q + fmha::kTiles * fmha::kBlockM - 1) / (fmha::kTiles * fmha::kBlockM);
   if (batch == 0 || total_q == 0 || pairs == 0) return FMHA_OK;  // nothing to compute
-  if (pairs > 65535) return FMHA_ERR_UNSUPPORTED;
+  // Rasterise in groups of kHeadGroup heads when one sequence's K/V does not fit
+  // in L2: the CTAs in flight then read the K/V of about kHeadGroup heads.
+  const int64_t kv_bytes = static_cast<int64_t>(kv_heads) * max_seqlen_k * head_dim * 4;  // K and V, bf16
+  const int head_group = (kv_bytes > kL2GroupBytes && heads > kHeadGroup) ? kHeadGroup : 0;
+  if (head_group == 0 ? pairs > 65535 : static_cast<int64_t>(heads) * pairs > INT32_MAX)
+    return FMHA_ERR_UNSUPPORTED;
 
   fmha::FwdParams p;
   // a k/v tensor with no rows still needs a valid map extent; it is never read then
@@ -123,7 +135,10 @@ extern "C" int fmha_fwd_gqa(const void* q, const void* k, const void* v, void* o
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.rescale_threshold = 8.0f;
 
-  dim3 grid(static_cast<unsigned>(heads), static_cast<unsigned>(pairs), static_cast<unsigned>(batch));
+  p.head_group = head_group;
+  const dim3 grid = head_group == 0
+                        ? dim3(static_cast<unsigned>(heads), static_cast<unsigned>(pairs), static_cast<unsigned>(batch))
+                        : dim3(static_cast<unsigned>(heads * pairs), static_cast<unsigned>(batch), 1u);
   return head_dim == 64 ? launch<64>(p, grid, stream) : launch<128>(p, grid, stream);
 }
 

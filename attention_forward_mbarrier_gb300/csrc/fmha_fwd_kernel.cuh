@@ -49,6 +49,7 @@ constexpr int kTiles = 2;      // query tiles per CTA
 // flight).  The slot-release protocol below relies on exactly four.
 constexpr int kStages = 4;
 constexpr int kThreads = 512;
+
 // A tile (128 rows: queries, keys or values) is stored as 64-column halves
 // of 128 rows x 128 bytes (16 KiB, 128-byte swizzle): one half for head_dim
 // 64, two for head_dim 128.
@@ -126,6 +127,8 @@ struct alignas(64) FwdParams {
   int batch, total_q, total_k, max_seqlen_q, max_seqlen_k, heads;
   int causal;
   int kv_group;             // query heads per K/V head (heads / kv_heads)
+  int head_group;           // 0: grid (heads, query blocks, batch); else heads per group of a
+                            // (heads x query blocks, batch) grid rasterised in head groups
   float scale_log2;         // scale * log2(e)
   float rescale_threshold;  // skip the O rescale while the max grew by <= this (log2 units)
 };
@@ -215,6 +218,35 @@ __device__ __forceinline__ int tile_blocks(int r0, int lq, int lk, int causal) {
   const int last = min(r0 + kBlockM - 1, lq - 1);
   const int lim = min(last + lk - lq, lk - 1);
   return lim >= 0 ? lim / kBlockN + 1 : 0;
+}
+
+// Work unit of this CTA: returns the head and sets the query block's
+// launch-order index and the sequence.  With head_group == 0 the grid is
+// (heads, query blocks, sequences).  Otherwise blockIdx.x runs over heads x
+// query blocks in groups of head_group heads: within a group the query blocks
+// go in launch order with the group's heads fastest, so the CTAs in flight
+// share the K/V of a few heads in L2 (used when one sequence's K/V exceeds
+// it).  The CTA index is read through opaque moves so that a second call
+// recomputes the head instead of keeping it in a register across the kernel.
+__device__ __forceinline__ int decode_unit(int heads, int head_group, int& launch_pair, int& b) {
+  uint32_t x, y, z, nx;
+  asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(x));
+  asm volatile("mov.u32 %0, %%ctaid.y;" : "=r"(y));
+  asm volatile("mov.u32 %0, %%ctaid.z;" : "=r"(z));
+  if (head_group == 0) {
+    launch_pair = static_cast<int>(y);
+    b = static_cast<int>(z);
+    return static_cast<int>(x);
+  }
+  asm volatile("mov.u32 %0, %%nctaid.x;" : "=r"(nx));
+  const int pairs = static_cast<int>(nx) / heads;
+  const int u = static_cast<int>(x);
+  const int g = u / (head_group * pairs);
+  const int gh = min(head_group, heads - g * head_group);  // heads in this (possibly last, partial) group
+  const int rem = u - g * head_group * pairs;
+  launch_pair = rem / gh;
+  b = static_cast<int>(y);
+  return g * head_group + (rem - launch_pair * gh);
 }
 
 __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
@@ -329,11 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     ptx::prefetch_tensormap(&p.tmap_v);
   }
 #ifdef FMHA_TRACE
+  const unsigned long long t_entry = static_cast<unsigned long long>(clock64());
   const size_t cta_lin = blockIdx.x + static_cast<size_t>(gridDim.x) * (blockIdx.y + static_cast<size_t>(gridDim.y) * blockIdx.z);
-  unsigned long long* trace_row = (g_trace != nullptr && blockIdx.x == 0 && blockIdx.z == 0)
-                                      ? g_trace + static_cast<size_t>(blockIdx.y) * kTraceSlots
-                                      : nullptr;
-  if (threadIdx.x == 0) FMHA_TRACE_AT(2);
   if (threadIdx.x == 0 && g_trace_ctas != nullptr) {
     g_trace_ctas[cta_lin * 4 + 0] = ptx::globaltimer_ns();
     uint32_t smid;
@@ -342,10 +371,16 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
   }
 #endif
 
-  // ---- work unit: head, 256-row query block, sequence
-  const int h = blockIdx.x;
-  const int pair = p.causal ? static_cast<int>(gridDim.y - 1 - blockIdx.y) : static_cast<int>(blockIdx.y);
-  const int b = blockIdx.z;
+  // ---- work unit: head, 256-row query block, sequence (see decode_unit)
+  int launch_pair, b;
+  const int h = decode_unit(p.heads, p.head_group, launch_pair, b);
+  const int pairs = p.head_group == 0 ? static_cast<int>(gridDim.y) : static_cast<int>(gridDim.x) / p.heads;
+  const int pair = p.causal ? pairs - 1 - launch_pair : launch_pair;
+#ifdef FMHA_TRACE
+  unsigned long long* trace_row =
+      (g_trace != nullptr && h == 0 && b == 0) ? g_trace + static_cast<size_t>(launch_pair) * kTraceSlots : nullptr;
+  if (threadIdx.x == 0 && trace_row != nullptr) trace_row[2] = t_entry;
+#endif
   int q0, lq, k0, lk;
   if (p.cu_q != nullptr) {
     q0 = p.cu_q[b];
@@ -515,6 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     // ---- epilogue of this tile: LSE and O / l -> bf16 (rows of the sequence only),
     // as soon as this tile's last PV completed
     const bool valid = active(t) && row < lq;
+    int lp_unused, b_unused;
+    const int h = decode_unit(p.heads, p.head_group, lp_unused, b_unused);  // recomputed: not held through the loop
     if (p.lse != nullptr && valid) {
       const float lse = (l > 0.f) ? (m_used * c + log2f(l)) * 0.69314718055994531f : -INFINITY;
       p.lse[static_cast<size_t>(h) * p.total_q + q0 + row] = lse;

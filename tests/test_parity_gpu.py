@@ -154,6 +154,14 @@ def test_long_sequence_sampled():
     check_sampled(wl.make_inputs(w, seed=22), n_random=96)
 
 
+def test_head_group_rasterisation_partial_group_sampled():
+    # one sequence whose K/V (6 heads x 34000 keys, ~104 MB) exceeds the
+    # head-group threshold: the grid is rasterised in groups of 4 heads, the
+    # last group holding 2
+    w = wl.varlen("long_h6_34000", (34000,), 6, causal=True)
+    check_sampled(wl.make_inputs(w, seed=24), n_random=96)
+
+
 def test_many_heads_sampled():
     # 256 heads: wide rows (heads x 256 bytes) in the tensor maps
     w = wl.dense("heads_256", 1, 700, 256, causal=False)
