@@ -64,7 +64,11 @@ enum fmha_status_code {
  *              reads cu_seqlens on the host.
  * max_seqlen_q an upper bound on every sequence's query / key length, as in
  * max_seqlen_k the page's varlen call (the caller's responsibility; a longer
- *              sequence is not fully computed).
+ *              sequence is not fully computed).  The launch has one CTA per
+ *              head, 256-query-row block and sequence: FMHA_ERR_UNSUPPORTED
+ *              if ceil(max_seqlen_q / 256) > 65535, or, when one sequence's
+ *              K/V exceeds 96 MiB (the grid is then ordered in head groups),
+ *              if heads * ceil(max_seqlen_q / 256) > 2^31 - 1.
  * heads        >= 1.
  * head_dim     64 or 128 (else FMHA_ERR_UNSUPPORTED).  The pages' runs use
  *              128; 64 is the adjacent size their command line also takes.
