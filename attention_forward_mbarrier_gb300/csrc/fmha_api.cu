@@ -48,22 +48,20 @@ bool make_map(CUtensorMap* m, const void* ptr, int tokens, int heads, int head_d
   return r == CUDA_SUCCESS;
 }
 
-// Head-group rasterisation: heads per group, and the per-sequence K/V size
-// above which it is used (a little under the 129 MB L2, which also holds the
-// Q and O streams).
-constexpr int kHeadGroup = 4;
+// Per-sequence K/V size above which the head-grouped grid order is used (a
+// little under the 129 MB L2, which also holds the Q and O streams).
 constexpr int64_t kL2GroupBytes = int64_t(96) << 20;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-template <int HD>
+template <int HD, bool kGrouped>
 int configure_kernel() {
   static int rc = -1;
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   // per-process attribute; re-applied cheaply if a previous attempt failed
   if (rc != 0) {
-    rc = cudaFuncSetAttribute(fmha::fmha_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    rc = cudaFuncSetAttribute(fmha::fmha_fwd_kernel<HD, kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(fmha::Dims<HD>::kSmemBytes)) == cudaSuccess
              ? 0
              : 1;
@@ -71,11 +69,11 @@ int configure_kernel() {
   return rc;
 }
 
-template <int HD>
+template <int HD, bool kGrouped>
 int launch(const fmha::FwdParams& p, dim3 grid, fmha_stream_t stream) {
-  if (configure_kernel<HD>() != 0) return FMHA_ERR_CUDA;
-  fmha::fmha_fwd_kernel<HD><<<grid, fmha::kThreads, fmha::Dims<HD>::kSmemBytes,
-                              reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  if (configure_kernel<HD, kGrouped>() != 0) return FMHA_ERR_CUDA;
+  fmha::fmha_fwd_kernel<HD, kGrouped><<<grid, fmha::kThreads, fmha::Dims<HD>::kSmemBytes,
+                                        reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
 }
 
@@ -110,9 +108,8 @@ extern "C" int fmha_fwd_gqa(const void* q, const void* k, const void* v, void* o
   // Rasterise in groups of kHeadGroup heads when one sequence's K/V does not fit
   // in L2: the CTAs in flight then read the K/V of about kHeadGroup heads.
   const int64_t kv_bytes = static_cast<int64_t>(kv_heads) * max_seqlen_k * head_dim * 4;  // K and V, bf16
-  const int head_group = (kv_bytes > kL2GroupBytes && heads > kHeadGroup) ? kHeadGroup : 0;
-  if (head_group == 0 ? pairs > 65535 : static_cast<int64_t>(heads) * pairs > INT32_MAX)
-    return FMHA_ERR_UNSUPPORTED;
+  const bool grouped = kv_bytes > kL2GroupBytes && heads > fmha::kHeadGroup;
+  if (grouped ? static_cast<int64_t>(heads) * pairs > INT32_MAX : pairs > 65535) return FMHA_ERR_UNSUPPORTED;
 
   fmha::FwdParams p;
   // a k/v tensor with no rows still needs a valid map extent; it is never read then
@@ -135,11 +132,12 @@ extern "C" int fmha_fwd_gqa(const void* q, const void* k, const void* v, void* o
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.rescale_threshold = 8.0f;
 
-  p.head_group = head_group;
-  const dim3 grid = head_group == 0
-                        ? dim3(static_cast<unsigned>(heads), static_cast<unsigned>(pairs), static_cast<unsigned>(batch))
-                        : dim3(static_cast<unsigned>(heads * pairs), static_cast<unsigned>(batch), 1u);
-  return head_dim == 64 ? launch<64>(p, grid, stream) : launch<128>(p, grid, stream);
+  if (grouped) {
+    const dim3 grid(static_cast<unsigned>(heads * pairs), static_cast<unsigned>(batch), 1u);
+    return head_dim == 64 ? launch<64, true>(p, grid, stream) : launch<128, true>(p, grid, stream);
+  }
+  const dim3 grid(static_cast<unsigned>(heads), static_cast<unsigned>(pairs), static_cast<unsigned>(batch));
+  return head_dim == 64 ? launch<64, false>(p, grid, stream) : launch<128, false>(p, grid, stream);
 }
 
 extern "C" int fmha_fwd(const void* q, const void* k, const void* v, void* out, float* lse,

@@ -127,8 +127,6 @@ struct alignas(64) FwdParams {
   int batch, total_q, total_k, max_seqlen_q, max_seqlen_k, heads;
   int causal;
   int kv_group;             // query heads per K/V head (heads / kv_heads)
-  int head_group;           // 0: grid (heads, query blocks, batch); else heads per group of a
-                            // (heads x query blocks, batch) grid rasterised in head groups
   float scale_log2;         // scale * log2(e)
   float rescale_threshold;  // skip the O rescale while the max grew by <= this (log2 units)
 };
@@ -220,33 +218,27 @@ __device__ __forceinline__ int tile_blocks(int r0, int lq, int lk, int causal) {
   return lim >= 0 ? lim / kBlockN + 1 : 0;
 }
 
-// Work unit of this CTA: returns the head and sets the query block's
-// launch-order index and the sequence.  With head_group == 0 the grid is
-// (heads, query blocks, sequences).  Otherwise blockIdx.x runs over heads x
-// query blocks in groups of head_group heads: within a group the query blocks
-// go in launch order with the group's heads fastest, so the CTAs in flight
-// share the K/V of a few heads in L2 (used when one sequence's K/V exceeds
-// it).  The CTA index is read through opaque moves so that a second call
+// Heads per rasterisation group of the head-grouped grid order.
+constexpr int kHeadGroup = 4;
+
+// Work unit of a CTA in the head-grouped grid order, (heads x query blocks,
+// sequences): blockIdx.x runs over the query blocks of a group of kHeadGroup
+// heads in launch order, the group's heads fastest, so that the CTAs in
+// flight share the K/V of a few heads in L2 (used when one sequence's K/V
+// exceeds it).  Returns the head and sets the query block's launch-order index.
+// The CTA index is read through an opaque move so that a second call
 // recomputes the head instead of keeping it in a register across the kernel.
-__device__ __forceinline__ int decode_unit(int heads, int head_group, int& launch_pair, int& b) {
-  uint32_t x, y, z, nx;
+__device__ __forceinline__ int decode_grouped(int heads, int& launch_pair) {
+  uint32_t x, nx;
   asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(x));
-  asm volatile("mov.u32 %0, %%ctaid.y;" : "=r"(y));
-  asm volatile("mov.u32 %0, %%ctaid.z;" : "=r"(z));
-  if (head_group == 0) {
-    launch_pair = static_cast<int>(y);
-    b = static_cast<int>(z);
-    return static_cast<int>(x);
-  }
   asm volatile("mov.u32 %0, %%nctaid.x;" : "=r"(nx));
   const int pairs = static_cast<int>(nx) / heads;
   const int u = static_cast<int>(x);
-  const int g = u / (head_group * pairs);
-  const int gh = min(head_group, heads - g * head_group);  // heads in this (possibly last, partial) group
-  const int rem = u - g * head_group * pairs;
+  const int g = u / (kHeadGroup * pairs);
+  const int gh = min(kHeadGroup, heads - g * kHeadGroup);  // heads in this (possibly last, partial) group
+  const int rem = u - g * kHeadGroup * pairs;
   launch_pair = rem / gh;
-  b = static_cast<int>(y);
-  return g * head_group + (rem - launch_pair * gh);
+  return g * kHeadGroup + (rem - launch_pair * gh);
 }
 
 __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
@@ -339,7 +331,9 @@ __device__ __forceinline__ float exp_pass(const float (&s)[128], float c, float 
 }
 
 // ---------------------------------------------------------------------------
-template <int HD>
+// kGrouped: the head-grouped grid order (see decode_grouped); else the grid
+// is (heads, query blocks, sequences).
+template <int HD, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_constant__ FwdParams p) {
   using D = Dims<HD>;
   constexpr int kHeadDim = HD;
@@ -371,10 +365,19 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
   }
 #endif
 
-  // ---- work unit: head, 256-row query block, sequence (see decode_unit)
-  int launch_pair, b;
-  const int h = decode_unit(p.heads, p.head_group, launch_pair, b);
-  const int pairs = p.head_group == 0 ? static_cast<int>(gridDim.y) : static_cast<int>(gridDim.x) / p.heads;
+  // ---- work unit: head, 256-row query block (causal launches start with the
+  // last, longest one), sequence
+  int h, launch_pair, pairs, b;
+  if constexpr (kGrouped) {
+    h = decode_grouped(p.heads, launch_pair);
+    pairs = static_cast<int>(gridDim.x) / p.heads;
+    b = static_cast<int>(blockIdx.y);
+  } else {
+    h = static_cast<int>(blockIdx.x);
+    launch_pair = static_cast<int>(blockIdx.y);
+    pairs = static_cast<int>(gridDim.y);
+    b = static_cast<int>(blockIdx.z);
+  }
   const int pair = p.causal ? pairs - 1 - launch_pair : launch_pair;
 #ifdef FMHA_TRACE
   unsigned long long* trace_row =
@@ -550,8 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     // ---- epilogue of this tile: LSE and O / l -> bf16 (rows of the sequence only),
     // as soon as this tile's last PV completed
     const bool valid = active(t) && row < lq;
-    int lp_unused, b_unused;
-    const int h = decode_unit(p.heads, p.head_group, lp_unused, b_unused);  // recomputed: not held through the loop
+    int lp_unused;
+    // recomputed rather than held through the loop
+    const int h = kGrouped ? decode_grouped(p.heads, lp_unused) : static_cast<int>(blockIdx.x);
     if (p.lse != nullptr && valid) {
       const float lse = (l > 0.f) ? (m_used * c + log2f(l)) * 0.69314718055994531f : -INFINITY;
       p.lse[static_cast<size_t>(h) * p.total_q + q0 + row] = lse;
