@@ -58,6 +58,9 @@ GOOD = dict(q=0x1000, k=0x2000, v=0x3000, out=0x4000, lse=0x5000, cu_seqlens_q=0
     (dict(head_dim=96), binding.FMHA_ERR_UNSUPPORTED),
     (dict(head_dim=256), binding.FMHA_ERR_UNSUPPORTED),
     (dict(batch=70000), binding.FMHA_ERR_UNSUPPORTED),
+    # more than 65535 blocks of 256 query rows on the plain grid (this K/V of
+    # 4 heads stays under the head-grouped threshold)
+    (dict(max_seqlen_q=65535 * 256 + 1, total_q=2 * (65535 * 256 + 1)), binding.FMHA_ERR_UNSUPPORTED),
     # dense mode needs total == batch * max_seqlen
     (dict(cu_seqlens_q=0, cu_seqlens_k=0), binding.FMHA_ERR_INVALID_ARG),
 ])
