@@ -7,7 +7,6 @@ fallback.  torch is used for device memory and streams.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import threading
 from typing import Optional
@@ -33,6 +32,32 @@ class FmhaError(RuntimeError):
         super().__init__(f"{what}: {status_string(status)} ({status})" if what else status_string(status))
 
 
+def open_library(path: str):
+    """Load a build of the library at ``path`` and declare its C signatures."""
+    L = ctypes.CDLL(path)
+    L.fmha_fwd.restype = ctypes.c_int
+    L.fmha_fwd.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p,
+    ]
+    L.fmha_fwd_gqa.restype = ctypes.c_int
+    L.fmha_fwd_gqa.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p,
+    ]
+    L.fmha_get_device_status.restype = ctypes.c_int
+    L.fmha_get_device_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]
+    L.fmha_status_string.restype = ctypes.c_char_p
+    L.fmha_status_string.argtypes = [ctypes.c_int]
+    L.fmha_version.restype = ctypes.c_int
+    L.fmha_version.argtypes = []
+    return L
+
+
 def lib():
     """Load libfmha.so (raises if it has not been built)."""
     global _lib
@@ -41,28 +66,7 @@ def lib():
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
                                    "or attention_forward_mbarrier_gb300.build.build()")
-            L = ctypes.CDLL(LIB_PATH)
-            L.fmha_fwd.restype = ctypes.c_int
-            L.fmha_fwd.argtypes = [
-                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                ctypes.c_void_p, ctypes.c_void_p,
-                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p,
-            ]
-            L.fmha_fwd_gqa.restype = ctypes.c_int
-            L.fmha_fwd_gqa.argtypes = [
-                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                ctypes.c_void_p, ctypes.c_void_p,
-                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p,
-            ]
-            L.fmha_get_device_status.restype = ctypes.c_int
-            L.fmha_get_device_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]
-            L.fmha_status_string.restype = ctypes.c_char_p
-            L.fmha_status_string.argtypes = [ctypes.c_int]
-            L.fmha_version.restype = ctypes.c_int
-            L.fmha_version.argtypes = []
-            _lib = L
+            _lib = open_library(LIB_PATH)
     return _lib
 
 
@@ -86,30 +90,33 @@ def _stream(stream) -> Optional[int]:
 
 
 def fmha_fwd(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
-             max_seqlen_q, max_seqlen_k, heads, head_dim, scale, causal, stream=None) -> int:
+             max_seqlen_q, max_seqlen_k, heads, head_dim, scale, causal, stream=None, library=None) -> int:
     """The C entry point with the same arguments; tensors or raw pointers.
 
-    Returns the status code (FMHA_OK == 0).  See include/fmha.h.
+    Returns the status code (FMHA_OK == 0).  See include/fmha.h.  ``library``:
+    a handle from ``open_library`` (another build of the library), else the
+    in-tree one.
     """
-    return int(lib().fmha_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+    return int((library or lib()).fmha_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                               _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(batch), int(total_q),
                               int(total_k), int(max_seqlen_q), int(max_seqlen_k), int(heads),
                               int(head_dim), float(scale), int(causal), _stream(stream)))
 
 
 def fmha_fwd_gqa(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
-                 max_seqlen_q, max_seqlen_k, heads, kv_heads, head_dim, scale, causal, stream=None) -> int:
+                 max_seqlen_q, max_seqlen_k, heads, kv_heads, head_dim, scale, causal, stream=None,
+                 library=None) -> int:
     """The grouped-K/V-head C entry point; tensors or raw pointers.  Returns the status."""
-    return int(lib().fmha_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+    return int((library or lib()).fmha_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                                   _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(batch), int(total_q),
                                   int(total_k), int(max_seqlen_q), int(max_seqlen_k), int(heads),
                                   int(kv_heads), int(head_dim), float(scale), int(causal), _stream(stream)))
 
 
-def fmha_get_device_status(stream=None):
+def fmha_get_device_status(stream=None, library=None):
     """(status, detail): synchronises the stream and reads/clears the device status word."""
     detail = ctypes.c_int(0)
-    st = int(lib().fmha_get_device_status(_stream(stream), ctypes.byref(detail)))
+    st = int((library or lib()).fmha_get_device_status(_stream(stream), ctypes.byref(detail)))
     return st, int(detail.value)
 
 
@@ -125,13 +132,15 @@ def fmha_version() -> int:
     return int(lib().fmha_version())
 
 
-def attention_forward(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None,
-                      max_seqlen_k=None, scale=None, causal=False, out=None, lse=None,
+def attention_forward(q, k, v, scale, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None,
+                      max_seqlen_k=None, causal=False, out=None, lse=None,
                       return_lse=True, stream=None):
     """Convenience wrapper over ``fmha_fwd`` for CUDA torch tensors.
 
     q: [total_q, heads, 128] bf16 (or [b, s, heads, 128] dense); k/v likewise
     with kv_heads heads (kv_heads dividing heads: grouped K/V heads).
+    scale: the softmax scale, always given (e.g. 1/sqrt(head_dim)); no
+    default is applied.
     cu_seqlens_*: int32 CUDA tensors [batch + 1] or None (dense).  Allocates
     ``out`` ([total_q, heads, 128] bf16) and ``lse`` ([heads, total_q] fp32)
     with torch when not given.  Raises FmhaError on a non-OK status.
@@ -160,8 +169,6 @@ def attention_forward(q, k, v, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_
     for name, t in (("q", qf), ("k", kf), ("v", vf)):
         if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty_like(qf)
     if lse is None and return_lse:

@@ -302,11 +302,28 @@ __device__ __forceinline__ float row_max128(const float (&s)[128]) {
   return ptx::fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
 }
 
-// One softmax exp pass over a row of 128 scores with reference max m_ref:
-// P = 2^(s c - m_ref c) (one packed FMA per pair, ex2), bf16 pairs stored to
-// TMEM at t_s (64 columns); returns the row sum of P.
+// Row min, the same way: with a negative scale the largest scaled score
+// s * scale belongs to the smallest raw score s.
+__device__ __forceinline__ float row_min128(const float (&s)[128]) {
+  float mn[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float a = ptx::fmin3(s[32 * q + 0], s[32 * q + 1], s[32 * q + 2]);
+#pragma unroll
+    for (int k = 3; k < 31; k += 2) a = ptx::fmin3(a, s[32 * q + k], s[32 * q + k + 1]);
+    mn[q] = fminf(a, s[32 * q + 31]);
+  }
+  return ptx::fmin3(fminf(mn[0], mn[1]), mn[2], mn[3]);
+}
+
+// One softmax exp pass over a row of 128 scores with reference score m_ref
+// (the raw score whose scaled value is the row's largest): P = 2^(s c - m_ref c)
+// (one packed FMA per pair, ex2), bf16 pairs stored to TMEM at t_s (64
+// columns); returns the row sum of P.  Masked scores hold +-inf with the sign
+// that makes s c = -inf, so they give P = 0; m_ref is infinite only while
+// every score so far was masked.
 __device__ __forceinline__ float exp_pass(const float (&s)[128], float c, float m_ref, uint32_t t_s) {
-  const float neg_mc = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
+  const float neg_mc = isinf(m_ref) ? 0.f : -m_ref * c;
   const float2 c2 = make_float2(c, c);
   const float2 nm2 = make_float2(neg_mc, neg_mc);
   float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -494,10 +511,14 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     const uint32_t t_s = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16) + col_s(t);
     const int row = m0 + kBlockM * t + r;  // sequence-local query index
     const int nb = n_blk(t);
-    const float c = p.scale_log2;
+    const float c = p.scale_log2;  // nonzero: the launcher passes 2^-126 for a zero scale
+    // Softmax order is the order of s * c: for a negative scale the reference
+    // score is the row minimum and masked scores hold +inf (s * c = -inf).
+    const bool neg = c < 0.f;
+    const float s_mask = neg ? INFINITY : -INFINITY;
     const int key_end = p.causal ? min(row + off + 1, lk) : lk;  // this row's visible keys [0, key_end)
     const int tile_key_end = p.causal ? min(m0 + kBlockM * t + off + 1, lk) : lk;  // the tile's first row
-    float m_used = -INFINITY;
+    float m_used = s_mask;
     float l = 0.f;
     for (int j = 0; j < nb; ++j) {
       // S_t(j): step commit j for the step's last tile, else tile 0's own commit
@@ -515,16 +536,21 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         const int lim = key_end - c0;
 #pragma unroll
         for (int k = 0; k < 128; ++k)
-          if (k >= lim) s[k] = -INFINITY;
+          if (k >= lim) s[k] = s_mask;
       }
-      // block max; the max in use moves only when it grew by more than the
-      // threshold (lazy rescale; NaN when both are -inf: keep)
-      const float m_blk = row_max128(s);
+      // block max of s * c; the reference in use moves only when the scaled
+      // max grew by more than the threshold (lazy rescale; NaN while both are
+      // the mask value: keep)
+      float m_blk;
+      if (neg)
+        m_blk = row_min128(s);
+      else
+        m_blk = row_max128(s);
       const float m_ref = (m_blk - m_used) * c > p.rescale_threshold ? m_blk : m_used;
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 2);
       const float row_sum = exp_pass(s, c, m_ref, t_s);
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 3);
-      // m_used == -inf gives alpha 0 (its O rows and l are still 0)
+      // an infinite m_used (nothing visible yet) gives alpha 0 (its O rows and l are still 0)
       const float alpha = (m_ref == m_used) ? 1.f : ptx::ex2_approx((m_used - m_ref) * c);
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // Rescale this warp's O rows.  PV_t(j-1) has completed (S_t(j) is

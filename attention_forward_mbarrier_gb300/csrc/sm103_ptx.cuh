@@ -301,6 +301,12 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Pack two floats to bf16x2 (round to nearest even): lo in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t d;

@@ -72,7 +72,9 @@ enum fmha_status_code {
  * heads        >= 1.
  * head_dim     64 or 128 (else FMHA_ERR_UNSUPPORTED).  The pages' runs use
  *              128; 64 is the adjacent size their command line also takes.
- * scale        finite softmax scale, e.g. 1/sqrt(128); no default is applied.
+ * scale        finite softmax scale of any sign, e.g. 1/sqrt(128); no default
+ *              is applied.  scale = 0 gives every visible key the same weight
+ *              (O = mean of the visible V rows, LSE = log of their count).
  * causal       0 or 1.
  * stream       CUDA stream the kernel is enqueued on.
  *

@@ -53,8 +53,8 @@ GOOD = dict(q=0x1000, k=0x2000, v=0x3000, out=0x4000, lse=0x5000, cu_seqlens_q=0
     (dict(batch=-1), binding.FMHA_ERR_INVALID_ARG),
     (dict(causal=2), binding.FMHA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), binding.FMHA_ERR_INVALID_ARG),
-    (dict(scale=0.0), binding.FMHA_ERR_INVALID_ARG),
-    (dict(scale=-1.0), binding.FMHA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), binding.FMHA_ERR_INVALID_ARG),
+    (dict(scale=float("-inf")), binding.FMHA_ERR_INVALID_ARG),
     (dict(head_dim=96), binding.FMHA_ERR_UNSUPPORTED),
     (dict(head_dim=256), binding.FMHA_ERR_UNSUPPORTED),
     (dict(batch=70000), binding.FMHA_ERR_UNSUPPORTED),

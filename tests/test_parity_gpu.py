@@ -4,8 +4,10 @@ Tolerances (bf16 output, fp32 LSE): O max-abs <= 2e-2 and relative RMS
 (||dO|| / ||O_ref||) <= 1e-2; LSE abs <= 1e-3 where finite, and -inf exactly
 where the oracle gives -inf.  Small shapes are compared in full; the five
 named workloads at full size in the launch configuration the benchmark
-times, on every row for the small ones and on a seeded row sample (every
-sequence's first and last rows plus random rows) for the large ones.
+times, on every row for the three smaller ones and on a seeded row sample
+(every sequence's first and last rows plus random rows) for the two large
+ones.  Outputs start as a canary (NaN for O, 12345 for LSE): sampled runs
+also check on the device that no canary is left in any row of any sequence.
 """
 import numpy as np
 import pytest
@@ -36,25 +38,44 @@ def _gpu():
     assert st == binding.FMHA_OK, (st, detail)
 
 
-def run_gpu(inp, with_lse=True, canary=None):
+LSE_CANARY = 12345.0
+
+
+def run_gpu(inp, with_lse=True, canary=float("nan"), library=None):
+    """One call through the C ABI.  ``out`` starts as the canary (NaN) and
+    ``lse`` as LSE_CANARY, so a row the kernel never wrote stays visible."""
     w = inp.workload
     dev = torch.device("cuda:0")
     q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
     cq = None if inp.cu_seqlens_q is None else inp.cu_seqlens_q.to(dev)
     ck = None if inp.cu_seqlens_k is None else inp.cu_seqlens_k.to(dev)
-    out = torch.empty_like(q) if canary is None else torch.full_like(q, canary)
-    lse = torch.full((w.heads, w.total_q), 12345.0, dtype=torch.float32, device=dev) if with_lse else None
+    out = torch.full_like(q, canary)
+    lse = torch.full((w.heads, w.total_q), LSE_CANARY, dtype=torch.float32, device=dev) if with_lse else None
     if w.kv_heads is None:
         st = binding.fmha_fwd(q, k, v, out, lse, cq, ck, w.batch, w.total_q, w.total_k, w.max_seqlen_q,
                               w.max_seqlen_k, w.heads, w.head_dim, w.softmax_scale, int(w.causal),
-                              torch.cuda.current_stream())
+                              torch.cuda.current_stream(), library=library)
     else:
         st = binding.fmha_fwd_gqa(q, k, v, out, lse, cq, ck, w.batch, w.total_q, w.total_k, w.max_seqlen_q,
                                   w.max_seqlen_k, w.heads, w.n_kv_heads, w.head_dim, w.softmax_scale,
-                                  int(w.causal), torch.cuda.current_stream())
+                                  int(w.causal), torch.cuda.current_stream(), library=library)
     assert st == binding.FMHA_OK, binding.status_string(st)
     torch.cuda.synchronize()
     return out, lse
+
+
+def assert_every_row_written(w, out, lse):
+    """No canary left in any row that belongs to a sequence (checked on the
+    device over the whole output, not only on compared rows)."""
+    cq, _ = w.cu_seqlens()
+    covered = torch.zeros(w.total_q, dtype=torch.bool, device=out.device)
+    for b in range(w.batch):
+        covered[int(cq[b]):int(cq[b + 1])] = True
+    n_nan = int(torch.isnan(out[covered]).sum())
+    assert n_nan == 0, f"{n_nan} output elements never written"
+    if lse is not None:
+        n_lse = int((lse[:, covered] == LSE_CANARY).sum())
+        assert n_lse == 0, f"{n_lse} LSE entries never written"
 
 
 def compare(o_gpu, lse_gpu, o_ref, lse_ref):
@@ -86,6 +107,7 @@ def check_full(inp):
 def check_sampled(inp, n_random=384, seed=1):
     w = inp.workload
     out, lse = run_gpu(inp)
+    assert_every_row_written(w, out, lse)
     rows = wl.sample_rows(w, n_random=n_random, seed=seed)
     ref_o, ref_l = oracle.oracle_fwd(*inp.oracle_args(), rows=rows)
     tok, h = rows // w.heads, rows % w.heads
@@ -104,8 +126,13 @@ def test_c2_dense_b1_h16_s2225_full():
     check_full(wl.make_inputs(wl.C2, seed=0))
 
 
+def test_c3_varlen_causal_t8192_h32_full():
+    check_full(wl.make_inputs(wl.C3, seed=0))
+
+
 @pytest.mark.parametrize("w", [wl.C3, wl.C4, wl.C5], ids=lambda w: w.name)
 def test_large_workloads_sampled(w):
+    # every row written (whole output), seeded rows against the oracle
     check_sampled(wl.make_inputs(w, seed=0))
 
 
@@ -131,6 +158,34 @@ EDGE = [
 @pytest.mark.parametrize("w", EDGE, ids=lambda w: w.name)
 def test_edge_shapes(w):
     check_full(wl.make_inputs(w, seed=11))
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.0883883, -0.5], ids=["zero", "neg_default", "neg_sharp"])
+def test_nonpositive_scale(scale):
+    # scale 0: every visible key has the same weight (O = mean of the visible
+    # V rows, LSE = log of their count); a negative scale reverses the order
+    # of the scores (the row minimum leads the softmax)
+    w = wl.varlen("scale_" + str(scale), (1, 127, 300, 257), 2, causal=True, scale=scale,
+                  seqlens_k=(1, 127, 300, 257))
+    check_full(wl.make_inputs(w, seed=6))
+    wn = wl.dense("scale_dense_" + str(scale), 2, 200, 3, causal=False, scale=scale)
+    check_full(wl.make_inputs(wn, seed=7))
+
+
+def test_zero_scale_closed_form():
+    # the closed form itself, independent of the oracle: causal row i of a
+    # sequence is the running mean of V rows 0..i and LSE_i = log(i + 1)
+    w = wl.varlen("scale0_closed", (200, 129), 2, causal=True, scale=0.0)
+    inp = wl.make_inputs(w, seed=8)
+    out, lse = run_gpu(inp)
+    cq, _ = w.cu_seqlens()
+    for b in range(w.batch):
+        lo, hi = int(cq[b]), int(cq[b + 1])
+        vv = inp.v[lo:hi].double()
+        counts = torch.arange(1, hi - lo + 1, dtype=torch.float64)
+        mean = vv.cumsum(0) / counts[:, None, None]
+        assert float((out[lo:hi].cpu().double() - mean).abs().max()) <= O_MAX_ABS
+        assert float((lse[:, lo:hi].cpu().double() - counts.log()[None, :]).abs().max()) <= LSE_ABS
 
 
 def test_uniform_inputs_wide_scores():
@@ -327,6 +382,6 @@ def test_convenience_wrapper_dense_4d():
     q4 = inp.q.view(1, 128, 2, 128).cuda()
     k4 = inp.k.view(1, 128, 2, 128).cuda()
     v4 = inp.v.view(1, 128, 2, 128).cuda()
-    out, lse = binding.attention_forward(q4, k4, v4)
+    out, lse = binding.attention_forward(q4, k4, v4, w.softmax_scale)
     ref_o, ref_l = oracle.oracle_fwd(*inp.oracle_args())
     compare(out.view(128, 2, 128).float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
