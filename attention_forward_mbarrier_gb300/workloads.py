@@ -192,6 +192,36 @@ def make_inputs(w: Workload, seed: int = 0, dist: str = "randn") -> Inputs:
     return Inputs(w, q, k, v, cq, ck)
 
 
+def make_dout(w: Workload, seed: int = 0) -> torch.Tensor:
+    """Seeded upstream gradient dO for the backward pass: standard-normal bf16
+    [total_q, heads, head_dim] on the CPU, from its own generator (seeded with
+    seed + 0x5EED, so q, k, v of make_inputs keep their bytes)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 0x5EED)
+    return torch.randn((w.total_q, w.heads, w.head_dim), generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def sample_keys(w: Workload, n_random: int, seed: int = 2, edge_rows: int = 2) -> np.ndarray:
+    """Flattened (token * kv_heads + kv_head) key indices for a seeded sample:
+    every sequence's first and last ``edge_rows`` keys for every K/V head plus
+    ``n_random`` uniformly drawn (token, K/V head) pairs."""
+    rng = np.random.default_rng(seed)
+    picks = []
+    _, ck = w.cu_seqlens()
+    hk = w.n_kv_heads
+    for b in range(w.batch):
+        lo, hi = int(ck[b]), int(ck[b + 1])
+        toks = set(range(lo, min(hi, lo + edge_rows))) | set(range(max(lo, hi - edge_rows), hi))
+        for t in sorted(toks):
+            for h in range(hk):
+                picks.append(t * hk + h)
+    if w.total_k > 0 and n_random > 0:
+        toks = rng.integers(0, w.total_k, size=n_random)
+        hs = rng.integers(0, hk, size=n_random)
+        picks.extend((toks * hk + hs).tolist())
+    return np.unique(np.asarray(picks, dtype=np.int64))
+
+
 def sample_rows(w: Workload, n_random: int, seed: int = 1, edge_rows: int = 2) -> np.ndarray:
     """Flattened (token * heads + head) indices for a seeded row sample.
 

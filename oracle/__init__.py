@@ -24,9 +24,19 @@ regression: FlashAttention-4 SM100 forward kernel spills registers", section
 LSE = -inf.  Readings of points the pages leave open (LSE base, causal
 alignment for Lq != Lk, empty rows) are stated in ``fmha_oracle.c``.
 
-Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
-(closed forms, a library softmax, brute force, structural invariants and
-planted mistakes).
+A third function covers the backward pass:
+
+* ``oracle_bwd`` -- the fp64 C oracle in ``fmha_bwd_oracle.c``: the gradients
+  dQ, dK, dV of L = sum dO . O, written out by the chain rule through the
+  softmax (row statistics recomputed from q, k, v; nothing is taken from a
+  forward run).  Full outputs, or sampled query rows / key rows.
+
+Parity status: every function here is pinned: the forward ones by
+``tests/test_oracle_pins.py`` (closed forms, a library softmax, brute force,
+structural invariants and planted mistakes), the backward one by
+``tests/test_oracle_bwd_pins.py`` (central finite differences of a float64
+forward, closed forms at scale 0, sum rules, grouped heads against repeated
+heads, sample modes against full mode, planted mistakes).
 """
 from __future__ import annotations
 
@@ -41,17 +51,27 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fmha_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_BWD_SRC = os.path.join(_HERE, "fmha_bwd_oracle.c")
+_BWD_LIB_PATH = os.path.join(_HERE, "liboracle_bwd.so")
 _lock = threading.Lock()
 _lib = None
+_bwd_lib = None
 
 
-def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
-    """Compile the C oracle with gcc + OpenMP into a shared library."""
+def _compile(src: str, out: str, force: bool) -> str:
     if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
         return out
     cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", out, src, "-lm"]
     subprocess.run(cmd, check=True)
     return out
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the C oracles (forward, and backward when building the default
+    forward library) with gcc + OpenMP into shared libraries."""
+    if src == _SRC and out == _LIB_PATH:
+        _compile(_BWD_SRC, _BWD_LIB_PATH, force)
+    return _compile(src, out, force)
 
 
 def _load(path: str = _LIB_PATH):
@@ -211,3 +231,94 @@ def brute_force_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, ma
                     out[q0 + i][h][d] = sum(w * V[k0 + j][h // group][d] for j, w in weights) / z
                 lse[h][q0 + i] = math.log(z)
     return np.array(out, dtype=np.float64), np.array(lse, dtype=np.float64)
+
+
+# ---------------------------------------------------------------- backward pass
+def _load_bwd(path: str = _BWD_LIB_PATH):
+    lib = ctypes.CDLL(path)
+    fn = lib.oracle_fmha_bwd
+    fn.restype = ctypes.c_int
+    fn.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # q k v dout
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # dq dk dv
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,  # cu_q cu_k batch
+        ctypes.c_int64, ctypes.c_int64,  # total_q total_k
+        ctypes.c_int, ctypes.c_int,  # max_seqlen_q max_seqlen_k
+        ctypes.c_int, ctypes.c_int, ctypes.c_int,  # heads kv_heads head_dim
+        ctypes.c_double, ctypes.c_int,  # scale causal
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,  # rows n_rows keys n_keys
+        ctypes.c_int,  # n_threads
+    ]
+    return lib
+
+
+def bwd_lib():
+    """The loaded backward oracle library (built on first use)."""
+    global _bwd_lib
+    with _lock:
+        if _bwd_lib is None:
+            _compile(_BWD_SRC, _BWD_LIB_PATH, False)
+            _bwd_lib = _load_bwd()
+    return _bwd_lib
+
+
+def bwd_source_text() -> str:
+    with open(_BWD_SRC) as f:
+        return f.read()
+
+
+def load_bwd_variant(source_text: str, workdir: str):
+    """Compile C source text (a variant of ``fmha_bwd_oracle.c``) and load it."""
+    src = os.path.join(workdir, "bwd_variant.c")
+    out = os.path.join(workdir, "libbwd_variant.so")
+    with open(src, "w") as f:
+        f.write(source_text)
+    _compile(src, out, True)
+    return _load_bwd(out)
+
+
+def oracle_bwd(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seqlen_k,
+               scale, causal, rows=None, keys=None, want_dq=True, want_dkdv=True,
+               n_threads: int = 0, lib_handle=None):
+    """fp64 gradients (dq, dk, dv) of L = sum(dout * O) from the C backward oracle.
+
+    q, dout: [total_q, heads, head_dim] bf16 (numpy uint16 bits or torch bf16);
+    k, v: [total_k, kv_heads, head_dim].  Other arguments as ``oracle_fwd``.
+    rows: optional flattened query indices (token * heads + head) -> dq is
+    [n_rows, head_dim]; keys: optional flattened key indices
+    (token * kv_heads + kv_head) -> dk, dv are [n_keys, head_dim].  Parts not
+    wanted come back as None.
+    """
+    qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(dout)
+    total_q, heads, head_dim = qb.shape
+    total_k, kv_heads = kb.shape[0], kb.shape[1]
+    if gb.shape != qb.shape or kb.shape[2] != head_dim or vb.shape != kb.shape or heads % kv_heads:
+        raise ValueError("inconsistent shapes")
+    if (cu_seqlens_q is None) != (cu_seqlens_k is None):
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both be given or both be None")
+    cu_q = cu_k = None
+    if cu_seqlens_q is not None:
+        cu_q = np.ascontiguousarray(np.asarray(cu_seqlens_q, dtype=np.int32))
+        cu_k = np.ascontiguousarray(np.asarray(cu_seqlens_k, dtype=np.int32))
+    rows_arr = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    keys_arr = None if keys is None else np.ascontiguousarray(np.asarray(keys, dtype=np.int64))
+    dq = dk = dv = None
+    if want_dq:
+        dq = np.zeros((total_q, heads, head_dim) if rows_arr is None else (len(rows_arr), head_dim))
+    if want_dkdv:
+        shp = (total_k, kv_heads, head_dim) if keys_arr is None else (len(keys_arr), head_dim)
+        dk, dv = np.zeros(shp), np.zeros(shp)
+    handle = bwd_lib() if lib_handle is None else lib_handle
+
+    def ptr(a):
+        return None if a is None else a.ctypes.data
+
+    rc = handle.oracle_fmha_bwd(
+        ptr(qb), ptr(kb), ptr(vb), ptr(gb), ptr(dq), ptr(dk), ptr(dv), ptr(cu_q), ptr(cu_k),
+        int(batch), int(total_q), int(total_k), int(max_seqlen_q), int(max_seqlen_k),
+        int(heads), int(kv_heads), int(head_dim), float(scale), int(bool(causal)),
+        ptr(rows_arr), 0 if rows_arr is None else len(rows_arr),
+        ptr(keys_arr), 0 if keys_arr is None else len(keys_arr), int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_fmha_bwd rejected its arguments")
+    return dq, dk, dv

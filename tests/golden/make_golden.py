@@ -41,6 +41,25 @@ def main():
     with open(os.path.join(HERE, "oracle_tiny_d128.json"), "w") as f:
         json.dump(fixture, f, indent=0)
 
+    # backward pass: the same kind of case with grouped K/V heads and an upstream gradient
+    w = wl.varlen("golden_bwd_tiny", (5, 3), 2, head_dim=32, causal=True, seqlens_k=(5, 4), kv_heads=1)
+    inp = wl.make_inputs(w, seed=2025)
+    dout = wl.make_dout(w, seed=2025)
+    dq, dk, dv = oracle.oracle_bwd(inp.q, inp.k, inp.v, dout, *inp.oracle_args()[3:])
+    fixture = {
+        "about": "backward-oracle outputs for saved seeded inputs; written by make_golden.py",
+        "seqlens_q": list(w.seqlens_q), "seqlens_k": list(w.seqlens_k),
+        "heads": w.heads, "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "causal": w.causal,
+        "scale": w.softmax_scale,
+        "q_bf16_hex": bits_hex(inp.q), "k_bf16_hex": bits_hex(inp.k), "v_bf16_hex": bits_hex(inp.v),
+        "dout_bf16_hex": bits_hex(dout),
+        "dq": [repr(float(x)) for x in dq.ravel()],
+        "dk": [repr(float(x)) for x in dk.ravel()],
+        "dv": [repr(float(x)) for x in dv.ravel()],
+    }
+    with open(os.path.join(HERE, "oracle_bwd_tiny_d32.json"), "w") as f:
+        json.dump(fixture, f, indent=0)
+
 
 if __name__ == "__main__":
     main()

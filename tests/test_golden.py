@@ -42,3 +42,20 @@ def test_stored_inputs_match_seeded_generator():
     inp = wl.make_inputs(w, seed=2024)
     q = inp.q.view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(q, _decode(g["q_bf16_hex"], q.shape))
+
+
+def test_backward_oracle_reproduces_stored_fixture(oracle_mod):
+    with open(os.path.join(HERE, "golden", "oracle_bwd_tiny_d32.json")) as f:
+        g = json.load(f)
+    sq, sk, H, HK, D = g["seqlens_q"], g["seqlens_k"], g["heads"], g["kv_heads"], g["head_dim"]
+    q = _decode(g["q_bf16_hex"], (sum(sq), H, D))
+    k = _decode(g["k_bf16_hex"], (sum(sk), HK, D))
+    v = _decode(g["v_bf16_hex"], (sum(sk), HK, D))
+    dout = _decode(g["dout_bf16_hex"], (sum(sq), H, D))
+    cq = np.concatenate([[0], np.cumsum(sq)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(sk)]).astype(np.int32)
+    dq, dk, dv = oracle_mod.oracle_bwd(q, k, v, dout, cq, ck, len(sq), max(sq), max(sk), g["scale"],
+                                       g["causal"])
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        want = np.array([float(x) for x in g[name]]).reshape(got.shape)
+        assert np.max(np.abs(got - want)) <= 1e-13, name
