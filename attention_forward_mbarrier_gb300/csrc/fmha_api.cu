@@ -17,6 +17,7 @@
 
 #include "fmha.h"
 #include "fmha_fwd_kernel.cuh"
+#include "fmha_bwd_kernel.cuh"
 
 namespace {
 
@@ -157,6 +158,107 @@ extern "C" int fmha_fwd(const void* q, const void* k, const void* v, void* out, 
                         int head_dim, float scale, int causal, fmha_stream_t stream) {
   return fmha_fwd_gqa(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, max_seqlen_q,
                       max_seqlen_k, heads, heads, head_dim, scale, causal, stream);
+}
+
+namespace {
+
+template <typename Kernel>
+int set_smem(Kernel kernel, uint32_t bytes, int& rc, std::mutex& mu) {
+  std::lock_guard<std::mutex> lock(mu);
+  if (rc != 0)
+    rc = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) ==
+                 cudaSuccess
+             ? 0
+             : 1;
+  return rc;
+}
+
+int configure_bwd() {
+  static int rc_dq = -1, rc_kv = -1;
+  static std::mutex mu;
+  if (set_smem(fmha::bwd::fmha_bwd_dq_kernel, fmha::bwd::DqSmem::kBytes, rc_dq, mu) != 0) return 1;
+  return set_smem(fmha::bwd::fmha_bwd_dkdv_kernel, fmha::bwd::DkvSmem::kBytes, rc_kv, mu);
+}
+
+}  // namespace
+
+extern "C" size_t fmha_bwd_workspace_size(int heads, int total_q) {
+  if (heads < 0 || total_q < 0) return 0;
+  return static_cast<size_t>(heads) * static_cast<size_t>(total_q) * sizeof(float);
+}
+
+extern "C" int fmha_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, float* workspace,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int total_q,
+                        int total_k, int max_seqlen_q, int max_seqlen_k, int heads, int kv_heads, int head_dim,
+                        float scale, int causal, fmha_stream_t stream) {
+  // ---- validation: no GPU work before this point
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || dout == nullptr || lse == nullptr ||
+      dq == nullptr || dk == nullptr || dv == nullptr || workspace == nullptr)
+    return FMHA_ERR_INVALID_ARG;
+  if (heads < 1 || kv_heads < 1 || heads % kv_heads != 0) return FMHA_ERR_INVALID_ARG;
+  if ((cu_seqlens_q == nullptr) != (cu_seqlens_k == nullptr)) return FMHA_ERR_INVALID_ARG;
+  if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return FMHA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FMHA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FMHA_ERR_INVALID_ARG;
+  const void* p16[] = {q, k, v, out, dout, dq, dk, dv};
+  for (const void* x : p16)
+    if (!aligned(x, 16)) return FMHA_ERR_INVALID_ARG;
+  if (!aligned(lse, 4) || !aligned(workspace, 4)) return FMHA_ERR_INVALID_ARG;
+  if (cu_seqlens_q == nullptr) {
+    if (static_cast<int64_t>(batch) * max_seqlen_q != total_q ||
+        static_cast<int64_t>(batch) * max_seqlen_k != total_k)
+      return FMHA_ERR_INVALID_ARG;
+  }
+  if (head_dim != 128) return FMHA_ERR_UNSUPPORTED;
+  if (batch > 65535) return FMHA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(heads) * head_dim * 2 >= (int64_t(1) << 32)) return FMHA_ERR_UNSUPPORTED;
+  const int qblocks = (max_seqlen_q + fmha::kBlockM - 1) / fmha::kBlockM;
+  const int kblocks = (max_seqlen_k + fmha::kBlockN - 1) / fmha::kBlockN;
+  if (qblocks > 65535 || kblocks > 65535) return FMHA_ERR_UNSUPPORTED;
+  if (batch == 0 || (total_q == 0 && total_k == 0)) return FMHA_OK;
+
+  fmha::bwd::BwdParams p;
+  const int tq = total_q > 0 ? total_q : 1;  // a map needs a nonzero extent; it is never read then
+  const int tk = total_k > 0 ? total_k : 1;
+  if (!make_map(&p.tmap_q, q, tq, heads, head_dim) || !make_map(&p.tmap_do, dout, tq, heads, head_dim) ||
+      !make_map(&p.tmap_k, k, tk, kv_heads, head_dim) || !make_map(&p.tmap_v, v, tk, kv_heads, head_dim))
+    return FMHA_ERR_CUDA;
+  p.out = static_cast<const __nv_bfloat16*>(out);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.lse = lse;
+  p.dvec = workspace;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.batch = batch;
+  p.total_q = total_q;
+  p.total_k = total_k;
+  p.max_seqlen_q = max_seqlen_q;
+  p.max_seqlen_k = max_seqlen_k;
+  p.heads = heads;
+  p.kv_heads = kv_heads;
+  p.causal = causal;
+  p.kv_group = heads / kv_heads;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+
+  if (configure_bwd() != 0) return FMHA_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // dQ (and D = rowsum(dO * O) into the workspace) first, then dK / dV, which read D
+  if (qblocks > 0 && total_q > 0) {
+    fmha::bwd::fmha_bwd_dq_kernel<<<dim3(heads, qblocks, batch), fmha::bwd::kThreads, fmha::bwd::DqSmem::kBytes,
+                                    st>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
+  }
+  if (kblocks > 0 && total_k > 0) {
+    fmha::bwd::fmha_bwd_dkdv_kernel<<<dim3(kv_heads, kblocks, batch), fmha::bwd::kThreads,
+                                      fmha::bwd::DkvSmem::kBytes, st>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
+  }
+  return FMHA_OK;
 }
 
 extern "C" int fmha_get_device_status(fmha_stream_t stream, int* detail) {

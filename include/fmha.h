@@ -26,6 +26,7 @@
 #ifndef FMHA_H_
 #define FMHA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -106,6 +107,51 @@ int fmha_fwd_gqa(const void *q, const void *k, const void *v, void *out, float *
                  int batch, int total_q, int total_k,
                  int max_seqlen_q, int max_seqlen_k, int heads, int kv_heads, int head_dim,
                  float scale, int causal, fmha_stream_t stream);
+
+/*
+ * fmha_bwd -- gradients of the forward pass: dQ, dK, dV of L = sum(dO * O).
+ *
+ * The benchmark step of "[BUG] CuTe DSL 4.7/4.8 regression: FlashAttention-4
+ * SM100 forward kernel spills registers" (section "Steps/Code to reproduce
+ * bug") runs this pass after the varlen causal forward.  With
+ * P_ij = exp(scale * q_i . k_j - LSE_i) over the visible keys (0 elsewhere):
+ *
+ *   dV_j = sum_i P_ij dO_i               D_i   = dO_i . O_i
+ *   dS_ij = P_ij (dO_i . v_j - D_i)      dQ_i  = scale * sum_j dS_ij k_j
+ *                                        dK_j  = scale * sum_i dS_ij q_i
+ *
+ * summed over every query head that reads a K/V head (grouped K/V heads as
+ * in fmha_fwd_gqa).
+ *
+ * q, out, dout bf16 [total_q, heads, head_dim]; out and lse are the outputs
+ *              of fmha_fwd / fmha_fwd_gqa for these q, k, v (lse required).
+ * k, v         bf16 [total_k, kv_heads, head_dim].
+ * dq           bf16 [total_q, heads, head_dim]: rows of every sequence written.
+ * dk, dv       bf16 [total_k, kv_heads, head_dim]: keys of every sequence
+ *              written (0 for a key no query sees).
+ * workspace    fp32 device scratch of fmha_bwd_workspace_size(heads, total_q)
+ *              bytes, 4-byte aligned, owned by the caller; it receives D.  Its
+ *              contents on entry do not matter; two calls in flight at the
+ *              same time must not share it.
+ * All other arguments are those of fmha_fwd_gqa (kv_heads == heads for
+ * multi-head attention).  head_dim must be 128 (else FMHA_ERR_UNSUPPORTED);
+ * ceil(max_seqlen_q / 128) and ceil(max_seqlen_k / 128) at most 65535.
+ * Every 16-byte alignment rule of fmha_fwd applies to q, k, v, out, dout,
+ * dq, dk and dv.
+ *
+ * Two kernels are enqueued on `stream` (dQ and D first, then dK and dV); the
+ * call allocates nothing and never synchronises.  Returns as fmha_fwd does.
+ */
+int fmha_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout,
+             const float *lse, void *dq, void *dk, void *dv, float *workspace,
+             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+             int batch, int total_q, int total_k,
+             int max_seqlen_q, int max_seqlen_k, int heads, int kv_heads, int head_dim,
+             float scale, int causal, fmha_stream_t stream);
+
+/* Bytes of device workspace fmha_bwd needs: heads * total_q * 4 (0 for a
+ * negative argument). */
+size_t fmha_bwd_workspace_size(int heads, int total_q);
 
 /*
  * fmha_get_device_status -- synchronise `stream`, then read and clear the

@@ -115,3 +115,36 @@ def test_kernel_has_no_register_spills():
     assert m, rep
     assert all(a == "0" and b == "0" for a, b in m), rep
     assert "0 bytes stack frame" in rep
+
+
+BWD_GOOD = dict(q=0x1000, k=0x2000, v=0x3000, out=0x4000, dout=0x5000, lse=0x6000, dq=0x7000, dk=0x8000,
+                dv=0x9000, workspace=0xa000, cu_seqlens_q=0xb000, cu_seqlens_k=0xc000, batch=2, total_q=300,
+                total_k=300, max_seqlen_q=200, max_seqlen_k=200, heads=4, kv_heads=2, head_dim=128,
+                scale=0.088, causal=1, stream=0)
+
+
+@pytest.mark.parametrize("change,expected", [
+    (dict(lse=0), binding.FMHA_ERR_INVALID_ARG),          # the backward pass needs the forward's LSE
+    (dict(workspace=0), binding.FMHA_ERR_INVALID_ARG),
+    (dict(dout=0), binding.FMHA_ERR_INVALID_ARG),
+    (dict(dk=0x8008), binding.FMHA_ERR_INVALID_ARG),      # not 16-byte aligned
+    (dict(workspace=0xa002), binding.FMHA_ERR_INVALID_ARG),
+    (dict(kv_heads=3), binding.FMHA_ERR_INVALID_ARG),
+    (dict(cu_seqlens_q=0), binding.FMHA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.FMHA_ERR_INVALID_ARG),
+    (dict(causal=-1), binding.FMHA_ERR_INVALID_ARG),
+    (dict(head_dim=64), binding.FMHA_ERR_UNSUPPORTED),
+    (dict(max_seqlen_k=65536 * 128, total_k=2 * 65536 * 128), binding.FMHA_ERR_UNSUPPORTED),
+])
+def test_backward_invalid_arguments_rejected_on_host(lib, change, expected):
+    args = dict(BWD_GOOD)
+    args.update(change)
+    assert binding.fmha_bwd(**args) == expected
+
+
+def test_backward_workspace_size(lib):
+    assert binding.fmha_bwd_workspace_size(16, 32768) == 16 * 32768 * 4
+    assert binding.fmha_bwd_workspace_size(-1, 5) == 0
+    args = dict(BWD_GOOD)
+    args.update(batch=0, total_q=0, total_k=0, max_seqlen_q=0, max_seqlen_k=0)
+    assert binding.fmha_bwd(**args) == binding.FMHA_OK
