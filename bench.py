@@ -341,6 +341,68 @@ def kernel_only(w: wl.Workload, dev, peak: float, steps: int = 5, warmup: int = 
             "causal": w.causal}
 
 
+def backward_only(w: wl.Workload, dev, peak: float, steps: int = 5, warmup: int = 3,
+                  flush_mode: str = "write+read"):
+    """Time fmha_bwd (both of its kernels) with inputs, O and LSE resident, for
+    context.  Algorithmic FLOPs of the backward: five GEMM families (S, dP, dV,
+    dK, dQ) = 2.5x the forward's; the kernels' recomputation of S and dP for
+    dQ is not credited.  Also times one forward + backward step."""
+    from attention_forward_mbarrier_gb300 import binding
+
+    inp = wl.make_inputs(w, seed=0)
+    dO = wl.make_dout(w, seed=0)
+    q, k, v, g = (t.to(dev) for t in (inp.q, inp.k, inp.v, dO))
+    cq = None if inp.cu_seqlens_q is None else inp.cu_seqlens_q.to(dev)
+    ck = None if inp.cu_seqlens_k is None else inp.cu_seqlens_k.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.heads, w.total_q), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(max(1, binding.fmha_bwd_workspace_size(w.heads, w.total_q) // 4), dtype=torch.float32,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flusher = L2Flusher(dev, flush_mode) if input_bytes(w) < 2 * L2_BYTES else None
+
+    def fwd():
+        st = call_fwd(binding, w, q, k, v, out, lse, cq, ck, stream)
+        if st != binding.FMHA_OK:
+            raise RuntimeError(binding.status_string(st))
+
+    def bwd():
+        st = binding.fmha_bwd(q, k, v, out, g, lse, dq, dk, dv, ws, cq, ck, w.batch, w.total_q, w.total_k,
+                              w.max_seqlen_q, w.max_seqlen_k, w.heads, w.n_kv_heads, w.head_dim,
+                              w.softmax_scale, int(w.causal), stream)
+        if st != binding.FMHA_OK:
+            raise RuntimeError(binding.status_string(st))
+
+    def timed(fn):
+        ms = []
+        for i in range(warmup + steps):
+            if flusher is not None:
+                flusher.flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= warmup:
+                ms.append(e0.elapsed_time(e1))
+        return statistics.mean(ms)
+
+    fwd()
+    bwd_ms = timed(bwd)
+    step_ms = timed(lambda: (fwd(), bwd()))
+    st, detail = binding.fmha_get_device_status(stream)
+    if st != binding.FMHA_OK:
+        raise RuntimeError(f"device status {binding.status_string(st)} detail {detail}")
+    flops = 2.5 * w.flops()
+    tf = flops / (bwd_ms * 1e-3) / 1e12
+    del q, k, v, g, out, lse, dq, dk, dv, ws, flusher
+    torch.cuda.empty_cache()
+    return {"tflops": tf, "frac_of_peak": tf / peak, "ms": bwd_ms, "gflop": flops / 1e9, "causal": w.causal,
+            "launches": 2, "fwd_bwd_ms": step_ms,
+            "fwd_bwd_tflops": 3.5 * w.flops() / (step_ms * 1e-3) / 1e12}
+
+
 def run_ours(args, w, rank, world, local):
     from attention_forward_mbarrier_gb300 import binding
     from attention_forward_mbarrier_gb300 import build as _build
@@ -507,6 +569,10 @@ def run_ours(args, w, rank, world, local):
         known = {**wl.CONFIGS, **wl.EXTRA}
         line["secondary"] = {x: kernel_only(known[x], dev, peak, flush_mode=args.flush)
                              for x in args.secondary.split(",") if x}
+    if not args.no_secondary and args.secondary_bwd:
+        known = {**wl.CONFIGS, **wl.EXTRA}
+        line["secondary_bwd"] = {x: backward_only(known[x], dev, peak, flush_mode=args.flush)
+                                 for x in args.secondary_bwd.split(",") if x}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp, budget_s=args.ref_budget)
     print(json.dumps(line), flush=True)
@@ -526,6 +592,8 @@ def main():
     ap.add_argument("--secondary", default=",".join([wl.C3.name, wl.C4.name, wl.C5.name, wl.GQA_C3.name,
                                                      wl.D64_C5.name]),
                     help="comma-separated workloads timed kernel-only after the main line")
+    ap.add_argument("--secondary-bwd", default=",".join([wl.C2.name, wl.C3.name, wl.C4.name, wl.C5.name]),
+                    help="comma-separated workloads whose backward pass (fmha_bwd) is timed after the main line")
     ap.add_argument("--clock-window", type=float, default=1.0,
                     help="seconds of back-to-back launches before the timed region")
     ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per sample")
