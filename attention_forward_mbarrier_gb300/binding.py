@@ -20,8 +20,8 @@ FMHA_ERR_TIMEOUT = 4
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfmha.so")
 
 # exported symbols, in the order include/fmha.h declares them
-SYMBOLS = ("fmha_fwd", "fmha_fwd_gqa", "fmha_bwd", "fmha_bwd_workspace_size", "fmha_get_device_status",
-           "fmha_status_string", "fmha_version")
+SYMBOLS = ("fmha_fwd", "fmha_fwd_gqa", "fmha_bwd", "fmha_bwd_workspace_size", "fmha_bwd_noalloc",
+           "fmha_get_device_status", "fmha_status_string", "fmha_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -53,6 +53,9 @@ def open_library(path: str):
     L.fmha_bwd.restype = ctypes.c_int
     L.fmha_bwd.argtypes = [ctypes.c_void_p] * 12 + [ctypes.c_int] * 8 + [ctypes.c_float, ctypes.c_int,
                                                                          ctypes.c_void_p]
+    L.fmha_bwd_noalloc.restype = ctypes.c_int
+    L.fmha_bwd_noalloc.argtypes = [ctypes.c_void_p] * 11 + [ctypes.c_int] * 8 + [ctypes.c_float, ctypes.c_int,
+                                                                                ctypes.c_void_p]
     L.fmha_bwd_workspace_size.restype = ctypes.c_size_t
     L.fmha_bwd_workspace_size.argtypes = [ctypes.c_int, ctypes.c_int]
     L.fmha_get_device_status.restype = ctypes.c_int
@@ -126,6 +129,18 @@ def fmha_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, cu_seqlens_q, cu_se
     return int((library or lib()).fmha_bwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
         _ptr(workspace), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(batch), int(total_q), int(total_k),
+        int(max_seqlen_q), int(max_seqlen_k), int(heads), int(kv_heads), int(head_dim), float(scale),
+        int(causal), _stream(stream)))
+
+
+def fmha_bwd_noalloc(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, batch, total_q,
+                     total_k, max_seqlen_q, max_seqlen_k, heads, kv_heads, head_dim, scale, causal, stream=None,
+                     library=None) -> int:
+    """fmha_bwd for callers that cannot allocate: its scratch is a fixed array
+    inside the library (heads * total_q <= 2**21).  Returns the status."""
+    return int((library or lib()).fmha_bwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(batch), int(total_q), int(total_k),
         int(max_seqlen_q), int(max_seqlen_k), int(heads), int(kv_heads), int(head_dim), float(scale),
         int(causal), _stream(stream)))
 

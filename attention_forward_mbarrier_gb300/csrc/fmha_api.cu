@@ -261,6 +261,59 @@ extern "C" int fmha_bwd(const void* q, const void* k, const void* v, const void*
   return FMHA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// fmha_bwd_noalloc: fmha_bwd for callers that cannot allocate device memory
+// (code running where cudaMalloc is unavailable or forbidden, e.g. inside a
+// host allocator's own hooks, a plugin whose host owns all memory, or a
+// process that has reserved the whole device up front).  The backward pass's
+// one scratch buffer, D = rowsum(dO * O), then lives in the fixed array below,
+// which every GPU that loads this library holds until the process exits.
+namespace {
+
+constexpr size_t kStaticScratchFloats = size_t(1) << 21;  // 8 MiB: heads * total_q <= 2,097,152
+__device__ __align__(256) float g_bwd_static_scratch[kStaticScratchFloats];
+
+// The array's device address, looked up once per device with that device
+// current.  In host code the array's name is only a stand-in, never a device
+// address.
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+float* g_scratch_addr[kMaxDevices] = {};
+
+int static_scratch(float** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FMHA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (dev >= 0 && dev < kMaxDevices && g_scratch_addr[dev] != nullptr) {
+    *ptr = g_scratch_addr[dev];
+    return FMHA_OK;
+  }
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_bwd_static_scratch) != cudaSuccess || addr == nullptr) return FMHA_ERR_CUDA;
+  if (dev >= 0 && dev < kMaxDevices) g_scratch_addr[dev] = static_cast<float*>(addr);
+  *ptr = static_cast<float*>(addr);
+  return FMHA_OK;
+}
+
+}  // namespace
+
+extern "C" int fmha_bwd_noalloc(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                                const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
+                                const int32_t* cu_seqlens_k, int batch, int total_q, int total_k,
+                                int max_seqlen_q, int max_seqlen_k, int heads, int kv_heads, int head_dim,
+                                float scale, int causal, fmha_stream_t stream) {
+  if (heads < 1 || total_q < 0) return FMHA_ERR_INVALID_ARG;
+  if (static_cast<size_t>(heads) * static_cast<size_t>(total_q) > kStaticScratchFloats)
+    return FMHA_ERR_UNSUPPORTED;  // D would not fit the fixed scratch array
+  float* scratch = nullptr;
+  const int rc = static_scratch(&scratch);
+  if (rc != FMHA_OK) return rc;
+  // Nothing in the array needs to start at zero: the dQ kernel writes every
+  // entry of D that the dK/dV kernel then reads.
+  return fmha_bwd(q, k, v, out, dout, lse, dq, dk, dv, scratch, cu_seqlens_q, cu_seqlens_k, batch, total_q,
+                  total_k, max_seqlen_q, max_seqlen_k, heads, kv_heads, head_dim, scale, causal, stream);
+}
+
 extern "C" int fmha_get_device_status(fmha_stream_t stream, int* detail) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FMHA_ERR_CUDA;
   int word = 0;

@@ -154,6 +154,35 @@ int fmha_bwd(const void *q, const void *k, const void *v, const void *out, const
 size_t fmha_bwd_workspace_size(int heads, int total_q);
 
 /*
+ * fmha_bwd_noalloc -- fmha_bwd without the workspace argument, for callers
+ * that cannot allocate device memory: code that runs where cudaMalloc is
+ * unavailable or not allowed (inside an allocator's own hooks, a plugin whose
+ * host owns every byte of device memory, a process that reserved the whole
+ * device up front).  The pages have no counterpart of this entry point.
+ *
+ * The scratch that fmha_bwd takes from the caller (D, heads * total_q
+ * floats) lives instead in one fixed array of 8 MiB inside this library,
+ * which every GPU that loads the library holds until the process exits.
+ * heads * total_q must be at most 2,097,152 (2^21); a larger problem is
+ * refused with FMHA_ERR_UNSUPPORTED before any GPU work.  The call allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ * The first call on each device looks the array's device address up with
+ * that device current (cudaGetSymbolAddress); make that first call before
+ * any stream capture.  Every call shares the one array per device and leaves
+ * its contents behind (nothing in it has to start at zero), so calls whose
+ * work overlaps on the GPU race on it: issue them on one stream, or order
+ * them.  Arguments, outputs and return values are otherwise those of
+ * fmha_bwd.
+ */
+int fmha_bwd_noalloc(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                     const float *lse, void *dq, void *dk, void *dv,
+                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                     int batch, int total_q, int total_k,
+                     int max_seqlen_q, int max_seqlen_k, int heads, int kv_heads, int head_dim,
+                     float scale, int causal, fmha_stream_t stream);
+
+/*
  * fmha_get_device_status -- synchronise `stream`, then read and clear the
  * device status word of the current device.  Returns FMHA_OK if no kernel
  * reported a problem since the last call, FMHA_ERR_TIMEOUT if a pipeline wait
