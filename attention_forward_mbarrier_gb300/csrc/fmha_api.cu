@@ -2,8 +2,9 @@
 //
 // Validates arguments without touching the GPU, encodes the three TMA tensor
 // maps (Q, K, V viewed as 2-D [tokens, heads * head_dim] bf16, 64 x 128 boxes
-// with 128-byte swizzle), and launches the kernel for head_dim 64 or 128 one CTA per (head, 256-row query block,
-// sequence).  The kernel orders the units in groups of a few heads, and causal
+// with 128-byte swizzle), and launches the kernel for head_dim 64, 128 or 256:
+// one CTA per (head, 256-row query block, sequence), or 128-row blocks for
+// head_dim 256.  The kernel orders the units in groups of a few heads, and causal
 // launches walk query blocks from the last to the first so the longest units
 // start first.
 #include <cuda.h>
@@ -106,16 +107,19 @@ extern "C" int fmha_fwd_gqa(const void* q, const void* k, const void* v, void* o
         static_cast<int64_t>(batch) * max_seqlen_k != total_k)
       return FMHA_ERR_INVALID_ARG;
   }
-  if (head_dim != 64 && head_dim != 128) return FMHA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return FMHA_ERR_UNSUPPORTED;
   if (batch > 65535) return FMHA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(heads) * head_dim * 2 >= (int64_t(1) << 32)) return FMHA_ERR_UNSUPPORTED;
 
-  const int pairs = (max_seqlen_q + fmha::kTiles * fmha::kBlockM - 1) / (fmha::kTiles * fmha::kBlockM);
+  // query rows per CTA: two 128-row tiles, one for head_dim 256
+  const int unit_rows = (head_dim == 256 ? 1 : fmha::kTiles) * fmha::kBlockM;
+  const int pairs = (max_seqlen_q + unit_rows - 1) / unit_rows;
   if (batch == 0 || total_q == 0 || pairs == 0) return FMHA_OK;  // nothing to compute
   // Rasterise in groups of kHeadGroup heads when one sequence's K/V does not fit
   // in L2: the CTAs in flight then read the K/V of about kHeadGroup heads.
   const int64_t kv_bytes = static_cast<int64_t>(kv_heads) * max_seqlen_k * head_dim * 4;  // K and V, bf16
-  const bool grouped = kv_bytes > kL2GroupBytes && heads > fmha::kHeadGroup;
+  // (head_dim 256 keeps the plain order: its grouped variant would spill registers)
+  const bool grouped = head_dim != 256 && kv_bytes > kL2GroupBytes && heads > fmha::kHeadGroup;
   if (grouped ? static_cast<int64_t>(heads) * pairs > INT32_MAX : pairs > 65535) return FMHA_ERR_UNSUPPORTED;
 
   fmha::FwdParams p;
@@ -149,7 +153,8 @@ extern "C" int fmha_fwd_gqa(const void* q, const void* k, const void* v, void* o
     return head_dim == 64 ? launch<64, true>(p, grid, stream) : launch<128, true>(p, grid, stream);
   }
   const dim3 grid(static_cast<unsigned>(heads), static_cast<unsigned>(pairs), static_cast<unsigned>(batch));
-  return head_dim == 64 ? launch<64, false>(p, grid, stream) : launch<128, false>(p, grid, stream);
+  if (head_dim == 64) return launch<64, false>(p, grid, stream);
+  return head_dim == 128 ? launch<128, false>(p, grid, stream) : launch<256, false>(p, grid, stream);
 }
 
 extern "C" int fmha_fwd(const void* q, const void* k, const void* v, void* out, float* lse,

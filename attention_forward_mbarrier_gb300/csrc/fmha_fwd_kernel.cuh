@@ -44,10 +44,7 @@ namespace fmha {
 
 constexpr int kBlockM = 128;   // query rows per tile (MMA M)
 constexpr int kBlockN = 128;   // keys per block (MMA N of QK^T, K of PV)
-constexpr int kTiles = 2;      // query tiles per CTA
-// K/V ring: four slots, each holding one K or one V block (two key blocks in
-// flight).  The slot-release protocol below relies on exactly four.
-constexpr int kStages = 4;
+constexpr int kTiles = 2;      // query tiles per CTA (at most; barriers exist for both)
 constexpr int kThreads = 512;
 
 // A tile (128 rows: queries, keys or values) is stored as 64-column halves
@@ -55,17 +52,27 @@ constexpr int kThreads = 512;
 // 64, two for head_dim 128.
 constexpr uint32_t kHalfBytes = kBlockM * 64 * 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kNumBars = 14;
+constexpr uint32_t kNumBars = 16;
 static_assert(kNumBars * 8 <= 256, "barrier area");
 
-// Sizes that depend on the head dimension (64 or 128).  Shared memory map,
-// offsets from a 1024-byte aligned base: Q tiles, the K/V ring, barriers,
+// Sizes that depend on the head dimension (64, 128 or 256).  Shared memory
+// map, offsets from a 1024-byte aligned base: Q tiles, the K/V ring, barriers,
 // misc words.
+//   head_dim 64, 128: two query tiles per CTA, a K/V ring of four slots (two
+//     key blocks in flight), TMEM S0 S1 O0 O1 of 128 columns each.
+//   head_dim 256: one query tile per CTA (O alone takes 256 TMEM columns: S
+//     [0, 128), O [256, 512)), a ring of two 64 KiB slots (K_j, V_j).
+// The slot-release protocol (load idx reuses the slot of load idx - kStages,
+// freed by a step commit) holds for either ring: a K slot is refilled after
+// the QK^T that read it has committed and a V slot after its PV, so no
+// barrier is ever waited on more than one phase late.
 template <int HD>
 struct Dims {
-  static_assert(HD == 64 || HD == 128, "head_dim");
+  static_assert(HD == 64 || HD == 128 || HD == 256, "head_dim");
   static constexpr int kHeadDim = HD;
   static constexpr int kHalves = HD / 64;
+  static constexpr int kTiles = HD == 256 ? 1 : 2;   // query tiles per CTA
+  static constexpr int kStages = HD == 256 ? 2 : 4;  // K/V ring slots
   static constexpr uint32_t kTileBytes = kBlockM * HD * 2;  // one Q tile / K or V block
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = kOffQ + kTiles * kTileBytes;
@@ -82,13 +89,30 @@ struct Dims {
 // last tile of the step that its S is ready and the producer that the step's
 // ring slots are free.
 constexpr int kBarQFull = 0;     // [2]
-constexpr int kBarKVFull = 2;    // [kStages]
+constexpr int kBarKVFull = 2;    // [4] (the ring's slots)
 constexpr int kBarStepDone = 6;  // [2]  step commit n, alternating
 constexpr int kBarSFull0 = 8;    //      QK^T of tile 0 landed (tile 0 not the last tile)
 constexpr int kBarPVReady = 9;   // [2]  P of tile t stored (and its O rows rescaled)
 constexpr int kBarOFinal = 11;   // [2]  last PV of tile t complete
 constexpr int kBarMmaDone = 13;  //      every MMA retired
-static_assert(kBarMmaDone + 1 == static_cast<int>(kNumBars), "ids");
+constexpr int kBarPVPart = 14;   // [2]  first part of P of tile t stored (split hand-off only)
+static_assert(kBarPVPart + 2 == static_cast<int>(kNumBars), "ids");
+
+// P hand-off split ("Kernel Bottleneck Tuning", section "5. Tune the
+// producer->consumer handoff split"): the softmax stores P in four chunks of
+// 32 keys and signals after the first FMHA_P_SPLIT of them, so that the MMA
+// warp starts O += P V on those keys while the rest is exponentiated; 4 (the
+// default) is one hand-off after the whole row.
+#ifndef FMHA_P_SPLIT
+#define FMHA_P_SPLIT 4
+#endif
+constexpr int kPSplit = FMHA_P_SPLIT;
+static_assert(kPSplit >= 1 && kPSplit <= 4, "P split in quarters of the key block");
+// Safety contract of the split: the PV K-steps the MMA warp issues after the
+// first signal (16 keys each) must not reach past the keys the softmax stored
+// before it, or an MMA reads P columns not yet written.
+constexpr int kPvStepsBeforeFull = 2 * kPSplit;
+static_assert(kPvStepsBeforeFull * 16 <= kPSplit * 32, "P split: consumer ahead of producer");
 
 
 // Warpgroup of each role.  Warp w reaches TMEM lanes 32 (w % 4) .. + 31, so
@@ -115,6 +139,12 @@ constexpr uint64_t kWaitLimitNs = FMHA_WAIT_LIMIT_NS;  // per wait (1 s by defau
 // gives its registers to the softmax.
 constexpr int kRegsSoftmax = 200, kRegsIdle = 32, kRegsControl = 80;
 static_assert(2 * kRegsSoftmax + kRegsIdle + kRegsControl == 512, "register split");
+// head_dim 256 (one query tile): warpgroup 1 has no tile and idles too; its
+// registers go to the softmax warpgroup (eight 32-column O chunks in the
+// rescale and the epilogue) and to the control warpgroup (its MMA issuer holds
+// the descriptors of 16 K-steps per QK^T).
+constexpr int kRegsSoftmax1 = 224, kRegsIdle1 = 32, kRegsControl1 = 512 - kRegsSoftmax1 - 2 * kRegsIdle1;
+static_assert(kRegsControl1 % 8 == 0 && kRegsControl1 <= 256 && kRegsControl1 > 128, "register split, one tile");
 
 struct alignas(64) FwdParams {
   CUtensorMap tmap_q;  // [total_q, heads*128] bf16, box 64 x 128, 128B swizzle
@@ -262,6 +292,12 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr) {
 template <int HD>
 __device__ __forceinline__ void issue_qk(uint32_t tmem_d, uint64_t q_desc, uint64_t k_desc) {
   constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, kBlockN, false, false);
+  if constexpr (HD > 128) {
+    // 16 K-steps: keep the base + offset sums at issue time rather than
+    // hoisted out of the caller's loop (they would not fit the issuer's
+    // register budget)
+    asm volatile("" : "+l"(q_desc), "+l"(k_desc));
+  }
   ptx::mma_ss_imm<false>(tmem_d, q_desc, k_desc, idesc);
 #pragma unroll
   for (int k = 1; k < HD / 16; ++k) {
@@ -278,6 +314,7 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_d, uint64_t q_desc, uint6
 template <int HD>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint64_t v_desc, bool accumulate) {
   constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, HD, false, true);
+  if constexpr (HD > 128) asm volatile("" : "+l"(v_desc), "+r"(tmem_p));  // as in issue_qk
   if (accumulate)
     ptx::mma_ts_imm<true>(tmem_d, tmem_p, v_desc, idesc);
   else
@@ -347,6 +384,59 @@ __device__ __forceinline__ float exp_pass(const float (&s)[128], float c, float 
   return a.x + a.y;
 }
 
+// The exp pass in four 32-key chunks; after chunk kPSplit - 1, `before` runs
+// (the O rescale, which must precede the first PV), the stores so far are made
+// visible (wait::st, fence) and `signal` is called (split hand-off).  Running
+// the rescale there rather than before the pass keeps fewer scores live.
+template <typename Before, typename Signal>
+__device__ __forceinline__ float exp_pass_split(const float (&s)[128], float c, float m_ref, uint32_t t_s,
+                                                Before&& before, Signal&& signal) {
+  const float neg_mc = isinf(m_ref) ? 0.f : -m_ref * c;
+  const float2 c2 = make_float2(c, c);
+  const float2 nm2 = make_float2(neg_mc, neg_mc);
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int k = q * 32 + 2 * i;
+      const float2 x = __ffma2_rn(make_float2(s[k], s[k + 1]), c2, nm2);
+      const float p0 = ptx::ex2_approx(x.x);
+      const float p1 = ptx::ex2_approx(x.y);
+      acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
+      pk[i] = ptx::pack_bf16x2(p0, p1);
+    }
+    ptx::tmem_st16(t_s + 16u * q, pk);
+    if (q == kPSplit - 1 && q < 3) {
+      before();
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      signal();
+    }
+  }
+  const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+  const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+  const float2 a = __fadd2_rn(a01, a23);
+  return a.x + a.y;
+}
+
+// O (+)= P V over the PV K-steps [k0, k1) (16 keys each); the first K-step of a
+// key block accumulates unless `accumulate` is false.
+template <int HD>
+__device__ __forceinline__ void issue_pv_steps(uint32_t tmem_d, uint32_t tmem_p, uint64_t v_desc, bool accumulate,
+                                               int k0, int k1) {
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, HD, false, true);
+#pragma unroll
+  for (int k = 0; k < kBlockN / 16; ++k) {
+    if (k < k0 || k >= k1) continue;
+    if (k == 0 && !accumulate)
+      ptx::mma_ts_imm<false>(tmem_d, tmem_p, v_desc, idesc);
+    else
+      ptx::mma_ts_imm<true>(tmem_d, tmem_p + 8u * k, v_desc + ((2048u * k) >> 4), idesc);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // kGrouped: the head-grouped grid order (see decode_grouped); else the grid
 // is (heads, query blocks, sequences).
@@ -354,6 +444,7 @@ template <int HD, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_constant__ FwdParams p) {
   using D = Dims<HD>;
   constexpr int kHeadDim = HD;
+  constexpr int kStages = D::kStages;
   constexpr uint32_t kTileBytes = D::kTileBytes;
   constexpr uint32_t kOffQ = D::kOffQ, kOffKV = D::kOffKV, kOffBar = D::kOffBar, kOffMisc = D::kOffMisc;
   constexpr uint64_t kSlotDescStep = kTileBytes >> 4;
@@ -414,14 +505,14 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     lk = p.max_seqlen_k;
   }
   if (lk < 0) lk = 0;
-  const int m0 = pair * (kTiles * kBlockM);
+  const int m0 = pair * (D::kTiles * kBlockM);
   if (m0 >= lq) return;  // uniform across the CTA, before any shared state
 
   // key blocks per tile; causal rows see keys j <= i + (lk - lq)
   const int off = lk - lq;
   const int n_blk0 = tile_blocks(m0, lq, lk, p.causal);
-  const int n_blk1 = tile_blocks(m0 + kBlockM, lq, lk, p.causal);
-  const bool active1 = m0 + kBlockM < lq;  // tile 0 is active whenever the unit exists
+  const int n_blk1 = D::kTiles > 1 ? tile_blocks(m0 + kBlockM, lq, lk, p.causal) : 0;
+  const bool active1 = D::kTiles > 1 && m0 + kBlockM < lq;  // tile 0 is active whenever the unit exists
   const int n_kv = max(n_blk0, n_blk1);
   // The last tile of every KV step: tile 1 whenever it has blocks (it never has
   // fewer than tile 0: causal rows further down see more keys), else tile 0.
@@ -444,8 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       ptx::mbar_arrive_expect_tx(bar, kTileBytes);
       const uint32_t dst = base + kOffQ + t * kTileBytes;
       const int y = q0 + m0 + kBlockM * t;
-      ptx::tma_load_2d(dst, &p.tmap_q, bar, xh, y, pol);
-      if (D::kHalves == 2) ptx::tma_load_2d(dst + kHalfBytes, &p.tmap_q, bar, xh + 64, y, pol);
+#pragma unroll
+      for (int hf = 0; hf < D::kHalves; ++hf) ptx::tma_load_2d(dst + hf * kHalfBytes, &p.tmap_q, bar, xh + 64 * hf, y, pol);
     }
   };
   auto load_kv = [&](int idx, uint64_t pol) {
@@ -455,8 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     const uint32_t dst = base + kOffKV + slot * kTileBytes;
     const CUtensorMap* m = (idx & 1) ? &p.tmap_v : &p.tmap_k;
     const int y = k0 + kBlockN * (idx >> 1);
-    ptx::tma_load_2d(dst, m, bar, xkv, y, pol);
-    if (D::kHalves == 2) ptx::tma_load_2d(dst + kHalfBytes, m, bar, xkv + 64, y, pol);
+#pragma unroll
+    for (int hf = 0; hf < D::kHalves; ++hf) ptx::tma_load_2d(dst + hf * kHalfBytes, m, bar, xkv + 64 * hf, y, pol);
   };
   // ring loads issued before the CTA-wide set-up sync (the ring starts empty)
   const int early_loads = min(kStages, 2 * n_kv);
@@ -468,7 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       ptx::mbar_init(ctx.bar(kBarPVReady + t), 4);  // the tile's 4 softmax warps
       ptx::mbar_init(ctx.bar(kBarOFinal + t), 1);
     }
-    for (int s = 0; s < kStages; ++s) ptx::mbar_init(ctx.bar(kBarKVFull + s), 1);
+    for (int s = 0; s < 4; ++s) ptx::mbar_init(ctx.bar(kBarKVFull + s), 1);
+    for (int t = 0; t < kTiles; ++t) ptx::mbar_init(ctx.bar(kBarPVPart + t), 4);
     ptx::mbar_init(ctx.bar(kBarSFull0), 1);
     ptx::mbar_init(ctx.bar(kBarMmaDone), 1);
     *ctx.abort_flag = 0u;
@@ -503,9 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
 #endif
 
   const int wg = warp >> 2;
-  if (wg == kWgSoftmax0 || wg == kWgSoftmax0 + 1) {
+  if (wg == kWgSoftmax0 || (D::kTiles > 1 && wg == kWgSoftmax0 + 1)) {
     // =============================== softmax (tile t = wg)
-    ptx::setmaxnreg_inc<kRegsSoftmax>();
+    ptx::setmaxnreg_inc<(D::kTiles > 1 ? kRegsSoftmax : kRegsSoftmax1)>();
     const int t = wg - kWgSoftmax0;
     const int r = (warp & 3) * 32 + lane;  // row within the tile == TMEM lane
     const uint32_t t_s = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16) + col_s(t);
@@ -548,24 +640,36 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         m_blk = row_max128(s);
       const float m_ref = (m_blk - m_used) * c > p.rescale_threshold ? m_blk : m_used;
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 2);
-      const float row_sum = exp_pass(s, c, m_ref, t_s);
-      if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 3);
       // an infinite m_used (nothing visible yet) gives alpha 0 (its O rows and l are still 0)
       const float alpha = (m_ref == m_used) ? 1.f : ptx::ex2_approx((m_used - m_ref) * c);
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // Rescale this warp's O rows.  PV_t(j-1) has completed (S_t(j) is
-        // committed after it) and PV_t(j) waits for this warp's P hand-off.
-        const uint32_t t_o = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16) + col_o(t);
+      // Rescale this warp's O rows.  PV_t(j-1) has completed (S_t(j) is
+      // committed after it) and PV_t(j) waits for this warp's P hand-off (with
+      // a split hand-off, the first one: hence the rescale before that signal).
+      auto rescale_o = [&]() {
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          const uint32_t t_o = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16) + col_o(t);
 #pragma unroll
-        for (int cc = 0; cc < HD / 32; ++cc) {
-          float o[32];
-          ptx::tmem_ld32_wait(t_o + 32u * cc, o);
-          uint32_t u[32];
+          for (int cc = 0; cc < HD / 32; ++cc) {
+            float o[32];
+            ptx::tmem_ld32_wait(t_o + 32u * cc, o);
+            uint32_t u[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(o[i] * alpha);
-          ptx::tmem_st32(t_o + 32u * cc, u);
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(o[i] * alpha);
+            ptx::tmem_st32(t_o + 32u * cc, u);
+          }
         }
+      };
+      float row_sum;
+      if constexpr (kPSplit < 4) {
+        row_sum = exp_pass_split(s, c, m_ref, t_s, rescale_o, [&]() {
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVPart + t));
+        });
+      } else {
+        row_sum = exp_pass(s, c, m_ref, t_s);
+        rescale_o();
       }
+      if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 3);
       l = l * alpha + row_sum;
       m_used = m_ref;
       ptx::tmem_wait_st();
@@ -660,11 +764,14 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       }
       if (r == 0) FMHA_TRACE_AT(kTrEpilogue + 4 * t + 1);
     }
-  } else if (wg == kWgIdle) {
+  } else if (wg == kWgIdle || wg == kWgSoftmax0 + 1) {
     // =============================== idle (its registers go to the softmax)
-    ptx::setmaxnreg_dec<kRegsIdle>();
+    ptx::setmaxnreg_dec<(D::kTiles > 1 ? kRegsIdle : kRegsIdle1)>();
   } else {
-    ptx::setmaxnreg_dec<kRegsControl>();
+    if constexpr (D::kTiles > 1)
+      ptx::setmaxnreg_dec<kRegsControl>();
+    else
+      ptx::setmaxnreg_inc<kRegsControl1>();
     if (warp == kWarpProducer) {
       // =============================== TMA producer (continues after the early loads)
       if (lane == 0) {
@@ -732,13 +839,28 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
 #pragma unroll
             for (int t = 0; t < kTiles; ++t) {
               if (!ok || j >= n_blk(t)) continue;
+              if constexpr (kPSplit < 4) {
+                // split hand-off: the K-steps of the first P chunks after the
+                // first signal, the rest after the full one
+                if (!wait_bar(ctx, kBarPVPart + t, j & 1, kRoleMma)) {
+                  ok = false;
+                  break;
+                }
+                ptx::tc_fence_after();
+                issue_pv_steps<HD>(tmem + col_o(t), tmem + col_s(t), kv_desc_mn + kSlotDescStep * vslot, j > 0, 0,
+                                   kPvStepsBeforeFull);
+              }
               if (!wait_bar(ctx, kBarPVReady + t, j & 1, kRoleMma)) {
                 ok = false;
                 break;
               }
               if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 1 + 2 * t);
               ptx::tc_fence_after();
-              issue_pv<HD>(tmem + col_o(t), tmem + col_s(t), kv_desc_mn + kSlotDescStep * vslot, j > 0);
+              if constexpr (kPSplit < 4)
+                issue_pv_steps<HD>(tmem + col_o(t), tmem + col_s(t), kv_desc_mn + kSlotDescStep * vslot, j > 0,
+                                   kPvStepsBeforeFull, kBlockN / 16);
+              else
+                issue_pv<HD>(tmem + col_o(t), tmem + col_s(t), kv_desc_mn + kSlotDescStep * vslot, j > 0);
               if (j + 1 < n_blk(t)) {
                 if (!k_ready) {
                   if (!wait_bar(ctx, kBarKVFull + kslot, (kidx / kStages) & 1, kRoleMma)) {

@@ -545,6 +545,44 @@ bool alloc(long long** d_out, int** d_status, int n_ctas) {
 
 }  // namespace
 
+namespace {
+// Accuracy probe of exp2_poly2: y_poly[i] = exp2_poly2(x[i]), y_ref[i] = exp2f(x[i]).
+__global__ void exp2_poly_values(const float* x, float* y_poly, float* y_ref, int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float x1 = i + 1 < n ? x[i + 1] : 0.f;
+  const float2 y = ptx_probe::exp2_poly2(make_float2(x[i], x1));
+  y_poly[i] = y.x;
+  y_ref[i] = exp2f(x[i]);
+  if (i + 1 < n) {
+    y_poly[i + 1] = y.y;
+    y_ref[i + 1] = exp2f(x1);
+  }
+}
+}  // namespace
+
+// Evaluates the FMA-pipe exp2 of the exp-loop probe (and exp2f beside it) on
+// n host inputs; results to host arrays.  Returns 0, 1 on a bad argument, 2 on
+// a CUDA error.
+extern "C" int fmha_probe_exp2_poly(const float* x, float* y_poly, float* y_ref, int n) {
+  if (x == nullptr || y_poly == nullptr || y_ref == nullptr || n < 1) return 1;
+  float* d = nullptr;
+  const size_t bytes = sizeof(float) * static_cast<size_t>(n);
+  if (cudaMalloc(&d, 3 * bytes) != cudaSuccess) return 2;
+  int rc = 0;
+  if (cudaMemcpy(d, x, bytes, cudaMemcpyHostToDevice) != cudaSuccess) rc = 2;
+  if (rc == 0) {
+    const int pairs = (n + 1) / 2;
+    exp2_poly_values<<<(pairs + 255) / 256, 256>>>(d, d + n, d + 2 * static_cast<size_t>(n), n);
+    if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) rc = 2;
+  }
+  if (rc == 0 && (cudaMemcpy(y_poly, d + n, bytes, cudaMemcpyDeviceToHost) != cudaSuccess ||
+                  cudaMemcpy(y_ref, d + 2 * static_cast<size_t>(n), bytes, cudaMemcpyDeviceToHost) != cudaSuccess))
+    rc = 2;
+  cudaFree(d);
+  return rc;
+}
+
 extern "C" int fmha_microbench_alu(int which, int reps, long long* out_cycles, int n_ctas) {
   if (which < 0 || which > 4 || reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
   long long* d_out = nullptr;

@@ -59,6 +59,8 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
 }
 
 // 2-D tiled bulk tensor load global -> shared, completion counted in bytes on `bar`.
+// dst and bar are this CTA's own shared memory (a plain launch is a one-CTA
+// cluster, so the .shared::cluster form addresses this CTA); no multicast.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
                                             int32_t x, int32_t y, uint64_t cache_policy) {
   asm volatile(

@@ -41,9 +41,25 @@ def load():
     L.fmha_microbench_boundary.argtypes = [ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
     L.fmha_microbench_exp_loop.restype = ctypes.c_int
     L.fmha_microbench_exp_loop.argtypes = [ctypes.c_int] * 3 + [P, ctypes.c_int]
+    F = ctypes.POINTER(ctypes.c_float)
+    L.fmha_probe_exp2_poly.restype = ctypes.c_int
+    L.fmha_probe_exp2_poly.argtypes = [F, F, F, ctypes.c_int]
     L.fmha_microbench_tmem_ld.restype = ctypes.c_int
     L.fmha_microbench_tmem_ld.argtypes = [ctypes.c_int, P, ctypes.c_int]
     return L
+
+
+def exp2_poly_values(x):
+    """(poly, exp2f) of the probe's FMA-pipe exp2 on a float32 numpy array."""
+    import numpy as np
+
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    yp, yr = np.empty_like(x), np.empty_like(x)
+    F = ctypes.POINTER(ctypes.c_float)
+    rc = load().fmha_probe_exp2_poly(x.ctypes.data_as(F), yp.ctypes.data_as(F), yr.ctypes.data_as(F), len(x))
+    if rc != 0:
+        raise RuntimeError(f"fmha_probe_exp2_poly failed with {rc}")
+    return yp, yr
 
 
 def _median(fn, *args, n_ctas):

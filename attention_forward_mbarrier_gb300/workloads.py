@@ -142,7 +142,13 @@ GQA_C3 = varlen("gqa_varlen_causal_t8192_h32_kv8_docs4", linspace_docs(8192, 4),
 # head_dim 64 on the single-document causal 32768-token shape with 32 heads
 D64_C5 = varlen("d64_causal_t32768_h32_docs1", linspace_docs(32768, 1), 32, head_dim=64,
                 description="Single-document causal, 32768 tokens, 32 heads, head_dim 64")
-EXTRA = {GQA_C3.name: GQA_C3, D64_C5.name: D64_C5}
+# head_dim 256 (one 128-row query tile per CTA) on the dense h16 s2225 shape
+# and on the varlen causal 8192-token shape
+D256_C2 = dense("d256_dense_b1_h16_s2225", 1, 2225, 16, head_dim=256,
+                description="Dense non-causal, batch 1, heads 16, seq 2225, head_dim 256")
+D256_C3 = varlen("d256_varlen_causal_t8192_h32_docs4", linspace_docs(8192, 4), 32, head_dim=256,
+                 description="Varlen causal, 8192 packed tokens, 32 heads, 4 docs, head_dim 256")
+EXTRA = {GQA_C3.name: GQA_C3, D64_C5.name: D64_C5, D256_C2.name: D256_C2, D256_C3.name: D256_C3}
 
 
 @dataclass

@@ -590,7 +590,7 @@ def main():
                     help="L2 flush between timed steps (see L2Flusher)")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--secondary", default=",".join([wl.C3.name, wl.C4.name, wl.C5.name, wl.GQA_C3.name,
-                                                     wl.D64_C5.name]),
+                                                     wl.D64_C5.name, wl.D256_C2.name, wl.D256_C3.name]),
                     help="comma-separated workloads timed kernel-only after the main line")
     ap.add_argument("--secondary-bwd", default=",".join([wl.C2.name, wl.C3.name, wl.C4.name, wl.C5.name]),
                     help="comma-separated workloads whose backward pass (fmha_bwd) is timed after the main line")

@@ -39,7 +39,7 @@ typedef struct CUstream_st *fmha_stream_t;
 enum fmha_status_code {
     FMHA_OK = 0,
     FMHA_ERR_INVALID_ARG = 1, /* a null or misaligned pointer, inconsistent sizes */
-    FMHA_ERR_UNSUPPORTED = 2, /* a valid request this build does not handle (head_dim not 64 or 128) */
+    FMHA_ERR_UNSUPPORTED = 2, /* a valid request this build does not handle (e.g. head_dim not 64, 128, 256) */
     FMHA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, tensor map) */
     FMHA_ERR_TIMEOUT = 4      /* a device-side pipeline wait gave up (see fmha_get_device_status) */
 };
@@ -71,8 +71,9 @@ enum fmha_status_code {
  *              K/V exceeds 96 MiB (the grid is then ordered in head groups),
  *              if heads * ceil(max_seqlen_q / 256) > 2^31 - 1.
  * heads        >= 1.
- * head_dim     64 or 128 (else FMHA_ERR_UNSUPPORTED).  The pages' runs use
- *              128; 64 is the adjacent size their command line also takes.
+ * head_dim     64, 128 or 256 (else FMHA_ERR_UNSUPPORTED).  The pages' runs
+ *              use 128; 64 and 256 are adjacent sizes their command line also
+ *              takes.  head_dim 256 runs one 128-row query block per CTA.
  * scale        finite softmax scale of any sign, e.g. 1/sqrt(128); no default
  *              is applied.  scale = 0 gives every visible key the same weight
  *              (O = mean of the visible V rows, LSE = log of their count).

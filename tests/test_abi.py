@@ -56,7 +56,8 @@ GOOD = dict(q=0x1000, k=0x2000, v=0x3000, out=0x4000, lse=0x5000, cu_seqlens_q=0
     (dict(scale=float("inf")), binding.FMHA_ERR_INVALID_ARG),
     (dict(scale=float("-inf")), binding.FMHA_ERR_INVALID_ARG),
     (dict(head_dim=96), binding.FMHA_ERR_UNSUPPORTED),
-    (dict(head_dim=256), binding.FMHA_ERR_UNSUPPORTED),
+    (dict(head_dim=192), binding.FMHA_ERR_UNSUPPORTED),
+    (dict(head_dim=512), binding.FMHA_ERR_UNSUPPORTED),
     (dict(batch=70000), binding.FMHA_ERR_UNSUPPORTED),
     # more than 65535 blocks of 256 query rows on the plain grid (this K/V of
     # 4 heads stays under the head-grouped threshold)

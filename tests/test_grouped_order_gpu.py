@@ -40,6 +40,15 @@ def group_lib():
     assert st == binding.FMHA_OK, (st, detail)
 
 
+def test_head_dim_256_keeps_plain_order(group_lib):
+    # head_dim 256 runs the plain grid order even above the threshold
+    w = wl.varlen("grp_d256_plain", (1500, 300), 6, head_dim=256, causal=True)
+    inp = wl.make_inputs(w, seed=42)
+    out, lse = run_gpu(inp, library=group_lib)
+    ref_o, ref_l = oracle.oracle_fwd(*inp.oracle_args())
+    compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
+
+
 CASES = [
     # 6 heads: groups of 4 and 2; a one-token sequence
     wl.varlen("grp_causal_h6", (1500, 700, 1), 6, causal=True),

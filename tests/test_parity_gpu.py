@@ -242,6 +242,28 @@ def test_head_dim_64_workload_sampled():
     check_sampled(wl.make_inputs(wl.D64_C5, seed=0))
 
 
+# ---------------------------------------------------------------- head_dim 256
+D256 = [
+    wl.varlen("d256_ragged_causal", (1, 127, 128, 129, 255, 256, 257, 383), 2, head_dim=256, causal=True),
+    wl.varlen("d256_noncausal_lq_ne_lk", (70, 260), 3, head_dim=256, causal=False, seqlens_k=(500, 33)),
+    wl.varlen("d256_lq_gt_lk_causal", (300, 200, 5), 2, head_dim=256, causal=True, seqlens_k=(100, 450, 1)),
+    wl.dense("d256_dense_b2_h4_s1000", 2, 1000, 4, head_dim=256, causal=False),
+    wl.varlen("d256_gqa_causal_h8_kv2", (300, 513), 8, head_dim=256, causal=True, kv_heads=2),
+    wl.varlen("d256_sharp", (700, 300), 2, head_dim=256, causal=True, scale=0.3),
+    wl.varlen("d256_scale0", (200, 129), 2, head_dim=256, causal=True, scale=0.0),
+]
+
+
+@pytest.mark.parametrize("w", D256, ids=lambda w: w.name)
+def test_head_dim_256(w):
+    check_full(wl.make_inputs(w, seed=19))
+
+
+def test_head_dim_256_workloads():
+    check_full(wl.make_inputs(wl.D256_C2, seed=0))
+    check_sampled(wl.make_inputs(wl.D256_C3, seed=0))
+
+
 # ---------------------------------------------------------------- grouped K/V heads
 GQA = [
     wl.varlen("gqa_causal_h8_kv2", (1, 129, 300, 513), 8, causal=True, kv_heads=2),
