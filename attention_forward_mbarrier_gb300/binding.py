@@ -20,7 +20,7 @@ FMHA_ERR_TIMEOUT = 4
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfmha.so")
 
 # exported symbols, in the order include/fmha.h declares them
-SYMBOLS = ("fmha_fwd", "fmha_fwd_gqa", "fmha_bwd", "fmha_bwd_workspace_size", "fmha_bwd_noalloc",
+SYMBOLS = ("fmha_fwd", "fmha_fwd_gqa", "fmha_fwd_fp8pv", "fmha_fwd_fp8pv_workspace_size", "fmha_bwd", "fmha_bwd_workspace_size", "fmha_bwd_noalloc",
            "fmha_get_device_status", "fmha_status_string", "fmha_version")
 
 _lock = threading.Lock()
@@ -50,6 +50,11 @@ def open_library(path: str):
         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p,
     ]
+    L.fmha_fwd_fp8pv.restype = ctypes.c_int
+    L.fmha_fwd_fp8pv.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] * 8 + [ctypes.c_float, ctypes.c_int,
+                                                                               ctypes.c_void_p]
+    L.fmha_fwd_fp8pv_workspace_size.restype = ctypes.c_size_t
+    L.fmha_fwd_fp8pv_workspace_size.argtypes = [ctypes.c_int] * 4
     L.fmha_bwd.restype = ctypes.c_int
     L.fmha_bwd.argtypes = [ctypes.c_void_p] * 12 + [ctypes.c_int] * 8 + [ctypes.c_float, ctypes.c_int,
                                                                          ctypes.c_void_p]
@@ -120,6 +125,22 @@ def fmha_fwd_gqa(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, 
                                   _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(batch), int(total_q),
                                   int(total_k), int(max_seqlen_q), int(max_seqlen_k), int(heads),
                                   int(kv_heads), int(head_dim), float(scale), int(causal), _stream(stream)))
+
+
+def fmha_fwd_fp8pv(q, k, v, out, lse, workspace, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                   max_seqlen_q, max_seqlen_k, heads, kv_heads, head_dim, scale, causal, stream=None,
+                   library=None) -> int:
+    """The FP8 (e4m3) P V forward entry point; tensors or raw pointers.  Returns the status."""
+    return int((library or lib()).fmha_fwd_fp8pv(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace), _ptr(cu_seqlens_q),
+        _ptr(cu_seqlens_k), int(batch), int(total_q), int(total_k), int(max_seqlen_q), int(max_seqlen_k),
+        int(heads), int(kv_heads), int(head_dim), float(scale), int(causal), _stream(stream)))
+
+
+def fmha_fwd_fp8pv_workspace_size(batch, total_k, kv_heads, head_dim, library=None) -> int:
+    """Bytes of device workspace fmha_fwd_fp8pv needs."""
+    return int((library or lib()).fmha_fwd_fp8pv_workspace_size(int(batch), int(total_k), int(kv_heads),
+                                                                 int(head_dim)))
 
 
 def fmha_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, cu_seqlens_q, cu_seqlens_k, batch, total_q,

@@ -14,11 +14,13 @@
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <mutex>
 
 #include "fmha.h"
 #include "fmha_fwd_kernel.cuh"
 #include "fmha_bwd_kernel.cuh"
+#include "fmha_fp8_prepass.cuh"
 
 namespace {
 
@@ -62,14 +64,14 @@ constexpr int64_t kL2GroupBytes = FMHA_L2_GROUP_BYTES;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-template <int HD, bool kGrouped>
+template <int HD, bool kGrouped, bool kFp8 = false>
 int configure_kernel() {
   static int rc = -1;
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   // per-process attribute; re-applied cheaply if a previous attempt failed
   if (rc != 0) {
-    rc = cudaFuncSetAttribute(fmha::fmha_fwd_kernel<HD, kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    rc = cudaFuncSetAttribute(fmha::fmha_fwd_kernel<HD, kGrouped, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(fmha::Dims<HD>::kSmemBytes)) == cudaSuccess
              ? 0
              : 1;
@@ -77,13 +79,31 @@ int configure_kernel() {
   return rc;
 }
 
-template <int HD, bool kGrouped>
+template <int HD, bool kGrouped, bool kFp8 = false>
 int launch(const fmha::FwdParams& p, dim3 grid, fmha_stream_t stream) {
-  if (configure_kernel<HD, kGrouped>() != 0) return FMHA_ERR_CUDA;
-  fmha::fmha_fwd_kernel<HD, kGrouped><<<grid, fmha::kThreads, fmha::Dims<HD>::kSmemBytes,
-                                        reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  if (configure_kernel<HD, kGrouped, kFp8>() != 0) return FMHA_ERR_CUDA;
+  fmha::fmha_fwd_kernel<HD, kGrouped, kFp8><<<grid, fmha::kThreads, fmha::Dims<HD>::kSmemBytes,
+                                              reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
 }
+
+// e4m3 V^T [rows, kpad] bytes (keys contiguous), box 128 keys x 128 rows, 128B swizzle.
+bool make_map_vt(CUtensorMap* m, const void* ptr, int64_t rows, int64_t kpad) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kpad), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kpad)};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Workspace of the FP8 variant: per-K/V-head max |V| (float bits), then the
+// e4m3 V^T at a 256-byte boundary.
+size_t fp8_amax_bytes(int kv_heads) { return (static_cast<size_t>(kv_heads) * 4 + 255) / 256 * 256; }
 
 }  // namespace
 
@@ -155,6 +175,98 @@ extern "C" int fmha_fwd_gqa(const void* q, const void* k, const void* v, void* o
   const dim3 grid(static_cast<unsigned>(heads), static_cast<unsigned>(pairs), static_cast<unsigned>(batch));
   if (head_dim == 64) return launch<64, false>(p, grid, stream);
   return head_dim == 128 ? launch<128, false>(p, grid, stream) : launch<256, false>(p, grid, stream);
+}
+
+extern "C" size_t fmha_fwd_fp8pv_workspace_size(int batch, int total_k, int kv_heads, int head_dim) {
+  if (batch < 0 || total_k < 0 || kv_heads < 1 || head_dim < 1) return 0;
+  const int64_t kpad = fmha::fp8::padded_keys(total_k, batch);
+  return fp8_amax_bytes(kv_heads) + static_cast<size_t>(kv_heads) * head_dim * static_cast<size_t>(kpad);
+}
+
+extern "C" int fmha_fwd_fp8pv(const void* q, const void* k, const void* v, void* out, float* lse, void* workspace,
+                              const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int total_q,
+                              int total_k, int max_seqlen_q, int max_seqlen_k, int heads, int kv_heads,
+                              int head_dim, float scale, int causal, fmha_stream_t stream) {
+  // ---- validation: no GPU work before this point
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || workspace == nullptr)
+    return FMHA_ERR_INVALID_ARG;
+  if (heads < 1 || kv_heads < 1 || heads % kv_heads != 0) return FMHA_ERR_INVALID_ARG;
+  if ((cu_seqlens_q == nullptr) != (cu_seqlens_k == nullptr)) return FMHA_ERR_INVALID_ARG;
+  if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return FMHA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FMHA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FMHA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(workspace, 256) ||
+      (lse != nullptr && !aligned(lse, 4)))
+    return FMHA_ERR_INVALID_ARG;
+  if (cu_seqlens_q == nullptr) {
+    if (static_cast<int64_t>(batch) * max_seqlen_q != total_q ||
+        static_cast<int64_t>(batch) * max_seqlen_k != total_k)
+      return FMHA_ERR_INVALID_ARG;
+  }
+  if (head_dim != 128) return FMHA_ERR_UNSUPPORTED;
+  if (batch > 65535) return FMHA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(heads) * head_dim * 2 >= (int64_t(1) << 32)) return FMHA_ERR_UNSUPPORTED;
+  const int64_t kpad = fmha::fp8::padded_keys(total_k, batch);
+  if (kpad + fmha::kBlockN >= (int64_t(1) << 31)) return FMHA_ERR_UNSUPPORTED;  // TMA x coordinates are int32
+  const int pairs = (max_seqlen_q + fmha::kTiles * fmha::kBlockM - 1) / (fmha::kTiles * fmha::kBlockM);
+  if (batch == 0 || total_q == 0 || pairs == 0) return FMHA_OK;
+  const int64_t kv_bytes = static_cast<int64_t>(kv_heads) * max_seqlen_k * head_dim * 4;
+  const bool grouped = kv_bytes > kL2GroupBytes && heads > fmha::kHeadGroup;
+  if (grouped ? static_cast<int64_t>(heads) * pairs > INT32_MAX : pairs > 65535) return FMHA_ERR_UNSUPPORTED;
+
+  fmha::FwdParams p;
+  const int tk = total_k > 0 ? total_k : 1;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* amax = reinterpret_cast<uint32_t*>(ws);
+  uint8_t* vt = ws + fp8_amax_bytes(kv_heads);
+  if (!make_map(&p.tmap_q, q, total_q, heads, head_dim) || !make_map(&p.tmap_k, k, tk, kv_heads, head_dim) ||
+      !make_map(&p.tmap_v, v, tk, kv_heads, head_dim) ||
+      !make_map_vt(&p.tmap_vt, vt, static_cast<int64_t>(kv_heads) * head_dim, kpad > 0 ? kpad : 16))
+    return FMHA_ERR_CUDA;
+  p.v_amax_bits = amax;
+  p.kv_group = heads / kv_heads;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.batch = batch;
+  p.total_q = total_q;
+  p.total_k = total_k;
+  p.max_seqlen_q = max_seqlen_q;
+  p.max_seqlen_k = max_seqlen_k;
+  p.heads = heads;
+  p.causal = causal;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  if (std::fabs(p.scale_log2) < FLT_MIN) p.scale_log2 = std::signbit(scale) ? -FLT_MIN : FLT_MIN;
+  p.rescale_threshold = 8.0f;
+
+  // V -> e4m3 V^T (max |V| per K/V head, then quantise and transpose)
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  fmha::fp8::PrepassParams pp;
+  pp.v = static_cast<const __nv_bfloat16*>(v);
+  pp.amax_bits = amax;
+  pp.vt = vt;
+  pp.cu_k = cu_seqlens_k;
+  pp.batch = batch;
+  pp.total_k = total_k;
+  pp.max_seqlen_k = max_seqlen_k;
+  pp.kv_heads = kv_heads;
+  pp.head_dim = head_dim;
+  pp.kpad = kpad;
+  if (cudaMemsetAsync(amax, 0, static_cast<size_t>(kv_heads) * 4, st) != cudaSuccess) return FMHA_ERR_CUDA;
+  const int64_t rows = static_cast<int64_t>(total_k) * kv_heads;
+  if (rows > 0) {
+    const int64_t blocks = std::min<int64_t>((rows + 7) / 8, 152 * 16);
+    fmha::fp8::v_amax_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(pp);
+    if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
+  }
+  if (kpad > 0) {
+    fmha::fp8::v_quant_kernel<<<dim3(static_cast<unsigned>((kpad + 127) / 128), kv_heads), fmha::fp8::kQuantThreads,
+                                0, st>>>(pp);
+    if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
+  }
+  if (grouped) return launch<128, true, true>(p, dim3(static_cast<unsigned>(heads * pairs), batch, 1u), stream);
+  return launch<128, false, true>(p, dim3(heads, pairs, batch), stream);
 }
 
 extern "C" int fmha_fwd(const void* q, const void* k, const void* v, void* out, float* lse,

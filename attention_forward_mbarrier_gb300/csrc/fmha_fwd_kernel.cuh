@@ -159,6 +159,9 @@ struct alignas(64) FwdParams {
   int kv_group;             // query heads per K/V head (heads / kv_heads)
   float scale_log2;         // scale * log2(e)
   float rescale_threshold;  // skip the O rescale while the max grew by <= this (log2 units)
+  // FP8 PV variant only
+  const uint32_t* v_amax_bits;  // max |V| per K/V head (float bits)
+  CUtensorMap tmap_vt;          // e4m3 V^T [kv_heads * 128, kpad] bytes, box 128 x 128, 128B swizzle
 };
 
 __device__ int g_status;  // 0 = ok, else 1 + (role * 256 + barrier id) of the first expired wait
@@ -437,11 +440,67 @@ __device__ __forceinline__ void issue_pv_steps(uint32_t tmem_d, uint32_t tmem_p,
   }
 }
 
+// e4m3 pair (round to nearest, saturating to +-448): lo in bits 0..7.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// The exp pass of the FP8 variant: P = 2^(s c - m_ref c) as above, stored as
+// e4m3, four keys per 32-bit TMEM column (key 4 i + b in byte b of column i):
+// 32 columns at t_s.  P <= 2^8 (the lazy-rescale threshold) fits e4m3's 448.
+// Returns the row sum of the unrounded P.
+__device__ __forceinline__ float exp_pass_fp8(const float (&s)[128], float c, float m_ref, uint32_t t_s) {
+  const float neg_mc = isinf(m_ref) ? 0.f : -m_ref * c;
+  const float2 c2 = make_float2(c, c);
+  const float2 nm2 = make_float2(neg_mc, neg_mc);
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int k = half * 64 + 4 * i;
+      const float2 x0 = __ffma2_rn(make_float2(s[k], s[k + 1]), c2, nm2);
+      const float2 x1 = __ffma2_rn(make_float2(s[k + 2], s[k + 3]), c2, nm2);
+      const float p0 = ptx::ex2_approx(x0.x), p1 = ptx::ex2_approx(x0.y);
+      const float p2 = ptx::ex2_approx(x1.x), p3 = ptx::ex2_approx(x1.y);
+      acc[(2 * i) & 3] = __fadd2_rn(acc[(2 * i) & 3], make_float2(p0, p1));
+      acc[(2 * i + 1) & 3] = __fadd2_rn(acc[(2 * i + 1) & 3], make_float2(p2, p3));
+      pk[i] = pack_e4m3x2(p0, p1) | (pack_e4m3x2(p2, p3) << 16);
+    }
+    ptx::tmem_st16(t_s + 16u * half, pk);
+  }
+  const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+  const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+  const float2 a = __fadd2_rn(a01, a23);
+  return a.x + a.y;
+}
+
+// O (+)= P V with e4m3 operands: M=128 queries, N=128 head dims, K=128 keys in
+// 4 steps of 32.  P from TMEM (8 columns of four keys per step); V^T K-major
+// in shared memory (128 head-dim rows of 128 key bytes, 128-byte swizzle):
+// a step of 32 keys is 32 bytes along the row.
+__device__ __forceinline__ void issue_pv_fp8(uint32_t tmem_d, uint32_t tmem_p, uint64_t vt_desc, bool accumulate) {
+  constexpr uint32_t idesc = ptx::idesc_e4m3_f32(kBlockM, 128);
+  if (accumulate)
+    ptx::mma_ts_f8_imm<true>(tmem_d, tmem_p, vt_desc, idesc);
+  else
+    ptx::mma_ts_f8_imm<false>(tmem_d, tmem_p, vt_desc, idesc);
+#pragma unroll
+  for (int k = 1; k < kBlockN / 32; ++k) ptx::mma_ts_f8_imm<true>(tmem_d, tmem_p + 8u * k, vt_desc + ((32u * k) >> 4), idesc);
+}
+
 // ---------------------------------------------------------------------------
 // kGrouped: the head-grouped grid order (see decode_grouped); else the grid
 // is (heads, query blocks, sequences).
-template <int HD, bool kGrouped>
+// kFp8: O += P V with P and V in e4m3 (kind::f8f6f4); V comes from the
+// pre-pass's transposed e4m3 copy (tmap_vt), its per-head scale folds into the
+// epilogue's 1 / l.
+template <int HD, bool kGrouped, bool kFp8 = false>
 __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_constant__ FwdParams p) {
+  static_assert(!kFp8 || (HD == 128 && kPSplit == 4), "FP8 PV: head_dim 128, one P hand-off");
   using D = Dims<HD>;
   constexpr int kHeadDim = HD;
   constexpr int kStages = D::kStages;
@@ -461,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     ptx::prefetch_tensormap(&p.tmap_q);
     ptx::prefetch_tensormap(&p.tmap_k);
     ptx::prefetch_tensormap(&p.tmap_v);
+    if constexpr (kFp8) ptx::prefetch_tensormap(&p.tmap_vt);
   }
 #ifdef FMHA_TRACE
   const unsigned long long t_entry = static_cast<unsigned long long>(clock64());
@@ -542,8 +602,16 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
   auto load_kv = [&](int idx, uint64_t pol) {
     const int slot = idx % kStages;
     const uint32_t bar = ctx.bar(kBarKVFull + slot);
-    ptx::mbar_arrive_expect_tx(bar, kTileBytes);
     const uint32_t dst = base + kOffKV + slot * kTileBytes;
+    if constexpr (kFp8) {
+      if (idx & 1) {  // e4m3 V^T block: 128 head-dim rows of 128 key bytes at the sequence's padded start
+        ptx::mbar_arrive_expect_tx(bar, kTileBytes / 2);
+        const int x = static_cast<int>(16 * ((k0 + 15) / 16 + b)) + kBlockN * (idx >> 1);
+        ptx::tma_load_2d(dst, &p.tmap_vt, bar, x, (h / p.kv_group) * kHeadDim, pol);
+        return;
+      }
+    }
+    ptx::mbar_arrive_expect_tx(bar, kTileBytes);
     const CUtensorMap* m = (idx & 1) ? &p.tmap_v : &p.tmap_k;
     const int y = k0 + kBlockN * (idx >> 1);
 #pragma unroll
@@ -660,7 +728,10 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         }
       };
       float row_sum;
-      if constexpr (kPSplit < 4) {
+      if constexpr (kFp8) {
+        row_sum = exp_pass_fp8(s, c, m_ref, t_s);
+        rescale_o();
+      } else if constexpr (kPSplit < 4) {
         row_sum = exp_pass_split(s, c, m_ref, t_s, rescale_o, [&]() {
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVPart + t));
@@ -693,7 +764,12 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     if (active(t) && (nb == 0 || wait_bar_warp(ctx, kBarOFinal + t, 0, kRoleSoftmax))) {
       if (nb > 0) ptx::tc_fence_after();
       if (r == 0) FMHA_TRACE_AT(kTrEpilogue + 4 * t + 0);
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float v_scale = 1.f;  // FP8 variant: V was stored as V / s, s = max|V| / 448
+      if constexpr (kFp8) {
+        const float amax = __uint_as_float(p.v_amax_bits[h / p.kv_group]);
+        v_scale = amax > 0.f ? amax / 448.f : 1.f;
+      }
+      const float inv = l > 0.f ? v_scale / l : 0.f;
       const uint32_t t_o = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16) + col_o(t);
       // Whole warp inside the sequence: stage its 32 rows of O in this tile's Q
       // buffer (free once the tile's last MMA completed) in the 128-byte
@@ -859,6 +935,8 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
               if constexpr (kPSplit < 4)
                 issue_pv_steps<HD>(tmem + col_o(t), tmem + col_s(t), kv_desc_mn + kSlotDescStep * vslot, j > 0,
                                    kPvStepsBeforeFull, kBlockN / 16);
+              else if constexpr (kFp8)
+                issue_pv_fp8(tmem + col_o(t), tmem + col_s(t), kv_desc + kSlotDescStep * vslot, j > 0);
               else
                 issue_pv<HD>(tmem + col_o(t), tmem + col_s(t), kv_desc_mn + kSlotDescStep * vslot, j > 0);
               if (j + 1 < n_blk(t)) {

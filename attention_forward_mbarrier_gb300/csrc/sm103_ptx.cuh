@@ -196,6 +196,20 @@ __device__ __forceinline__ void mma_ts_imm(uint32_t d_tmem, uint32_t a_tmem, uin
                  : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f8f6f4 (the element types come
+// from the instruction descriptor).
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_ts_f8_imm(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
+  if (kAccumulate)
+    asm volatile("tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem), "r"(a_tmem),
+                 "l"(b_desc), "r"(idesc)
+                 : "memory");
+  else
+    asm volatile("tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, 0;" ::"r"(d_tmem), "r"(a_tmem),
+                 "l"(b_desc), "r"(idesc)
+                 : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 async op issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -226,6 +240,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
          | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16)  //
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0)
+// and fp32 D, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                                // D format: f32
+         | (0u << 7)                              // A format: e4m3
+         | (0u << 10)                             // B format: e4m3
+         | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane, waited for.

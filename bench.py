@@ -403,6 +403,46 @@ def backward_only(w: wl.Workload, dev, peak: float, steps: int = 5, warmup: int 
             "fwd_bwd_tflops": 3.5 * w.flops() / (step_ms * 1e-3) / 1e12}
 
 
+def fp8_call(w: wl.Workload, dev, peak: float, steps: int = 5, warmup: int = 3, flush_mode: str = "write+read"):
+    """Time the whole fmha_fwd_fp8pv call (V quantisation pre-pass + attention),
+    inputs resident, for context.  FLOPs are the forward's; the peak is the mixed
+    one (QK^T at the bf16 rate, PV at twice it: 4/3 of the bf16 peak)."""
+    from attention_forward_mbarrier_gb300 import binding
+
+    inp = wl.make_inputs(w, seed=0)
+    q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
+    cq = None if inp.cu_seqlens_q is None else inp.cu_seqlens_q.to(dev)
+    ck = None if inp.cu_seqlens_k is None else inp.cu_seqlens_k.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.heads, w.total_q), dtype=torch.float32, device=dev)
+    ws = torch.empty(binding.fmha_fwd_fp8pv_workspace_size(w.batch, w.total_k, w.n_kv_heads, w.head_dim),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flusher = L2Flusher(dev, flush_mode) if input_bytes(w) < 2 * L2_BYTES else None
+    ms = []
+    for i in range(warmup + steps):
+        if flusher is not None:
+            flusher.flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        st = binding.fmha_fwd_fp8pv(q, k, v, out, lse, ws, cq, ck, w.batch, w.total_q, w.total_k, w.max_seqlen_q,
+                                    w.max_seqlen_k, w.heads, w.n_kv_heads, w.head_dim, w.softmax_scale,
+                                    int(w.causal), stream)
+        e1.record(stream)
+        if st != binding.FMHA_OK:
+            raise RuntimeError(binding.status_string(st))
+        torch.cuda.synchronize()
+        if i >= warmup:
+            ms.append(e0.elapsed_time(e1))
+    mean = statistics.mean(ms)
+    tf = w.flops() / (mean * 1e-3) / 1e12
+    mixed_peak = peak * 4.0 / 3.0
+    del q, k, v, out, lse, ws, flusher
+    torch.cuda.empty_cache()
+    return {"tflops": tf, "frac_of_mixed_peak": tf / mixed_peak, "mixed_peak": mixed_peak, "ms": mean,
+            "launches": 3, "includes": "V max + e4m3 quantise/transpose pre-pass + attention"}
+
+
 def run_ours(args, w, rank, world, local):
     from attention_forward_mbarrier_gb300 import binding
     from attention_forward_mbarrier_gb300 import build as _build
@@ -573,6 +613,10 @@ def run_ours(args, w, rank, world, local):
         known = {**wl.CONFIGS, **wl.EXTRA}
         line["secondary_bwd"] = {x: backward_only(known[x], dev, peak, flush_mode=args.flush)
                                  for x in args.secondary_bwd.split(",") if x}
+    if not args.no_secondary and args.secondary_fp8:
+        known = {**wl.CONFIGS, **wl.EXTRA}
+        line["secondary_fp8pv"] = {x: fp8_call(known[x], dev, peak, flush_mode=args.flush)
+                                   for x in args.secondary_fp8.split(",") if x}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp, budget_s=args.ref_budget)
     print(json.dumps(line), flush=True)
@@ -594,6 +638,8 @@ def main():
                     help="comma-separated workloads timed kernel-only after the main line")
     ap.add_argument("--secondary-bwd", default=",".join([wl.C2.name, wl.C3.name, wl.C4.name, wl.C5.name]),
                     help="comma-separated workloads whose backward pass (fmha_bwd) is timed after the main line")
+    ap.add_argument("--secondary-fp8", default=",".join([wl.C2.name, wl.C3.name, wl.C5.name]),
+                    help="comma-separated workloads timed through fmha_fwd_fp8pv after the main line")
     ap.add_argument("--clock-window", type=float, default=1.0,
                     help="seconds of back-to-back launches before the timed region")
     ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per sample")

@@ -110,6 +110,44 @@ int fmha_fwd_gqa(const void *q, const void *k, const void *v, void *out, float *
                  float scale, int causal, fmha_stream_t stream);
 
 /*
+ * fmha_fwd_fp8pv -- fmha_fwd_gqa with the O += P V product on FP8 (e4m3)
+ * operands, after "Kernel Bottleneck Tuning" (sections "4. If scheduling has
+ * no headroom: eliminate instructions algebraically" and "5. Tune the
+ * producer->consumer handoff split"), whose attention forward runs P V in
+ * FP8.  Opt-in: the result is less accurate than fmha_fwd's.
+ *
+ * P is rounded to e4m3 after the exponent (P <= 2^8 by the lazy-rescale
+ * threshold, inside e4m3's range); V is rounded to e4m3 as V / s with one scale
+ * s = max|V| / 448 per K/V head, folded into the epilogue's 1 / l; the row sum
+ * l and the LSE use the unrounded P (the LSE is as accurate as fmha_fwd's).
+ * Expected error of O against exact attention: relative RMS a few 1e-2, and
+ * at most about 2^-3 * max|V| for any element (half an e4m3 unit on P and on V).
+ *
+ * workspace    device memory of fmha_fwd_fp8pv_workspace_size(batch, total_k,
+ *              kv_heads, head_dim) bytes, 256-byte aligned, owned by the
+ *              caller, contents on entry irrelevant.  The call writes into it:
+ *              at offset 0, max|V| per K/V head as float bits; at offset
+ *              ceil(kv_heads * 4 / 256) * 256, the e4m3 values of V / s as
+ *              [kv_heads][head_dim][kpad] bytes with keys contiguous, sequence
+ *              b's key i at column 16 * (ceil(k0(b) / 16) + b) + i (k0(b) its
+ *              first key token, kpad = 16 * (ceil(total_k / 16) + batch)) and
+ *              zeros between sequences.  Calls that share a workspace must
+ *              not overlap on the GPU.
+ * head_dim     128 (else FMHA_ERR_UNSUPPORTED).
+ * All other arguments, return values and errors are those of fmha_fwd_gqa.
+ * Three kernels are enqueued on `stream` (max |V|, quantise and transpose V,
+ * attention) after a cudaMemsetAsync of the max words; nothing is allocated.
+ */
+int fmha_fwd_fp8pv(const void *q, const void *k, const void *v, void *out, float *lse, void *workspace,
+                   const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                   int batch, int total_q, int total_k,
+                   int max_seqlen_q, int max_seqlen_k, int heads, int kv_heads, int head_dim,
+                   float scale, int causal, fmha_stream_t stream);
+
+/* Bytes of workspace fmha_fwd_fp8pv needs (0 for an invalid argument). */
+size_t fmha_fwd_fp8pv_workspace_size(int batch, int total_k, int kv_heads, int head_dim);
+
+/*
  * fmha_bwd -- gradients of the forward pass: dQ, dK, dV of L = sum(dO * O).
  *
  * The benchmark step of "[BUG] CuTe DSL 4.7/4.8 regression: FlashAttention-4

@@ -149,3 +149,34 @@ def test_backward_workspace_size(lib):
     args = dict(BWD_GOOD)
     args.update(batch=0, total_q=0, total_k=0, max_seqlen_q=0, max_seqlen_k=0)
     assert binding.fmha_bwd(**args) == binding.FMHA_OK
+
+
+FP8_GOOD = dict(q=0x1000, k=0x2000, v=0x3000, out=0x4000, lse=0x5000, workspace=0x10000, cu_seqlens_q=0x6000,
+                cu_seqlens_k=0x7000, batch=2, total_q=300, total_k=300, max_seqlen_q=200, max_seqlen_k=200,
+                heads=4, kv_heads=2, head_dim=128, scale=0.088, causal=1, stream=0)
+
+
+@pytest.mark.parametrize("change,expected", [
+    (dict(workspace=0), binding.FMHA_ERR_INVALID_ARG),
+    (dict(workspace=0x10010), binding.FMHA_ERR_INVALID_ARG),  # not 256-byte aligned
+    (dict(v=0x3008), binding.FMHA_ERR_INVALID_ARG),
+    (dict(kv_heads=3), binding.FMHA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), binding.FMHA_ERR_INVALID_ARG),
+    (dict(head_dim=64), binding.FMHA_ERR_UNSUPPORTED),
+    (dict(head_dim=256), binding.FMHA_ERR_UNSUPPORTED),
+])
+def test_fp8_invalid_arguments_rejected_on_host(lib, change, expected):
+    args = dict(FP8_GOOD)
+    args.update(change)
+    assert binding.fmha_fwd_fp8pv(**args) == expected
+
+
+def test_fp8_workspace_size(lib):
+    # per-head max words padded to 256 bytes, then kv_heads * head_dim rows of
+    # 16 * (ceil(total_k / 16) + batch) bytes
+    assert binding.fmha_fwd_fp8pv_workspace_size(4, 8192, 32, 128) == 256 + 32 * 128 * 16 * (512 + 4)
+    assert binding.fmha_fwd_fp8pv_workspace_size(1, 1, 80, 128) == 512 + 80 * 128 * 32
+    assert binding.fmha_fwd_fp8pv_workspace_size(-1, 5, 1, 128) == 0
+    args = dict(FP8_GOOD)
+    args.update(batch=0, total_q=0, total_k=0, max_seqlen_q=0, max_seqlen_k=0)
+    assert binding.fmha_fwd_fp8pv(**args) == binding.FMHA_OK
