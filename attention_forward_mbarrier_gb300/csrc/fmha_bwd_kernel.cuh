@@ -15,11 +15,16 @@
 //   fmha_bwd_dq_kernel    one CTA per (head, 128 query rows, sequence): first
 //                         D_i (written to the workspace for the second kernel),
 //                         then per 128-key block S = Q K^T and dP = dO V^T into
-//                         TMEM, dS in bf16 over S, dQ += dS K.
+//                         TMEM, dS in bf16 over S, dQ += dS K; S is
+//                         double-buffered and dP released as soon as it is in
+//                         registers, so the next blocks' products overlap the
+//                         gradient math.
 //   fmha_bwd_dkdv_kernel  one CTA per (K/V head, 128 keys, sequence): per query
-//                         block of every query head of the group, S^T = K Q^T
-//                         and dP^T = V dO^T into TMEM, P^T and dS^T in bf16 over
-//                         them, dV += P^T dO and dK += dS^T Q.
+//                         block of every query head of the group, in two
+//                         halves of 64 queries, S^T = K Q^T and dP^T = V dO^T
+//                         into TMEM, P^T and dS^T in bf16 over them, dV += P^T
+//                         dO and dK += dS^T Q; one half's gradient math
+//                         overlaps the other half's products.
 // Every GEMM is a tcgen05.mma of one of the forward's two forms: both operands
 // K-major in shared memory, or A from TMEM with an MN-major B.  Warp roles
 // (192 threads): warps 0-3 the gradient math on one TMEM lane (row) each and
@@ -80,28 +85,44 @@ __device__ __forceinline__ void seq_bounds(const BwdParams& p, int b, int& q0, i
 __device__ __forceinline__ float neg_lse2(float lse) { return lse == -INFINITY ? -INFINITY : -lse * kLog2e; }
 
 // ============================================================================ dQ
-// Shared memory: Q, dO tiles, a 2-stage ring of (K, V) blocks, barriers.
+// Shared memory: Q and dO tiles, a 3-slot ring of K blocks and a 2-slot ring
+// of V blocks, barriers.
 struct DqSmem {
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffDo = kTile;
-  static constexpr uint32_t kOffRing = 2 * kTile;  // stage s: K at + 2 s kTile, V at + (2 s + 1) kTile
-  static constexpr uint32_t kOffBar = kOffRing + 4 * kTile;
+  static constexpr uint32_t kOffK = 2 * kTile;  // slot s at + s kTile (3 slots)
+  static constexpr uint32_t kOffV = 5 * kTile;  // slot s at + s kTile (2 slots)
+  static constexpr uint32_t kOffBar = 7 * kTile;
   static constexpr uint32_t kOffMisc = kOffBar + 128;
   static constexpr uint32_t kBytes = kOffBar + 256 + 1024;
   static_assert(kBytes <= 232448, "shared memory per CTA");
 };
+constexpr int kDqKSlots = 3, kDqVSlots = 2;
 // barrier ids
-constexpr int kDqQFull = 0;      // Q and dO landed
-constexpr int kDqKVFull = 1;     // [2] K_j, V_j of stage j & 1 landed
-constexpr int kDqStageFree = 3;  // [2] the MMAs reading stage s retired
-constexpr int kDqSReady = 5;     // S(j), dP(j) in TMEM
-constexpr int kDqPReady = 6;     // dS(j) stored (4 warps)
-constexpr int kDqDone = 7;       // every MMA retired
-// TMEM columns.  The bf16 pairs of a 32-column chunk of S (or dP) are stored
-// over columns 16 c .. 16 c + 15 of the same tensor, which the chunk loads of
-// this row have already read.
-constexpr uint32_t kDqColS = 0, kDqColDp = 128, kDqColDq = 256;
+constexpr int kDqQFull = 0;     // Q and dO landed
+constexpr int kDqKFull = 1;     // [3] K_j of slot j % 3 landed
+constexpr int kDqVFull = 4;     // [2] V_j of slot j % 2 landed
+constexpr int kDqKFree = 6;     // [3] dQ(j) retired: K_j no longer read
+constexpr int kDqBlkReady = 9;  // [2] S(j) and dP(j) in TMEM, barrier j & 1; also tells the
+                                // producer that V_j (read only by dP(j)) is free
+constexpr int kDqDpFree = 11;   // dP(j) read into registers (4 warps)
+constexpr int kDqPReady = 12;   // [2] dS(j) stored, barrier j & 1 (4 warps)
+constexpr int kDqDone = 14;     // every MMA retired
+// Pairs of alternating barriers where a waiter could otherwise find a barrier
+// two phases on: dP(j+1) lets the gradient warps finish block j+1 before the
+// MMA thread polls for dS(j), and dP(j+1) may retire before the producer polls
+// for dP(j).  With two barriers the next phase of each needs a step the waiter
+// itself has not yet allowed.
+// TMEM columns: S of block j at 128 (j & 1) (dS as bf16 over its first 64
+// columns, chunk c of 32 scores to columns 16 c .. 16 c + 15, already read),
+// dP at 256, dQ at 384.
+constexpr uint32_t kDqColDp = 256, kDqColDq = 384;
+__device__ __forceinline__ uint32_t dq_col_s(int j) { return 128u * static_cast<uint32_t>(j & 1); }
 
+// Schedule (one MMA-issuing thread): S(0), dP(0), S(1); then per block j:
+// dP(j+1) as soon as the gradient warps have dP(j) in registers, dQ(j) once
+// dS(j) is stored, S(j+2) into the S buffer dQ(j) just read.  The gradient
+// math of block j thus overlaps dP(j+1) and the S products of later blocks.
 __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -131,27 +152,35 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
   ctx.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + DqSmem::kOffMisc + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + DqSmem::kOffMisc);
 
-  auto load_kv = [&](int j, uint64_t pol) {
-    const int s = j & 1;
-    const uint32_t bar = ctx.bar(kDqKVFull + s);
-    ptx::mbar_arrive_expect_tx(bar, 2 * kTile);
-    const uint32_t dk = base + DqSmem::kOffRing + 2u * s * kTile;
-    const int y = k0 + kBlockN * j;
-    ptx::tma_load_2d(dk, &p.tmap_k, bar, xkv, y, pol);
-    ptx::tma_load_2d(dk + kHalfBytes, &p.tmap_k, bar, xkv + 64, y, pol);
-    ptx::tma_load_2d(dk + kTile, &p.tmap_v, bar, xkv, y, pol);
-    ptx::tma_load_2d(dk + kTile + kHalfBytes, &p.tmap_v, bar, xkv + 64, y, pol);
+  auto load_tile = [&](const CUtensorMap* m, uint32_t dst, uint32_t bar, int x, int y, uint64_t pol) {
+    ptx::tma_load_2d(dst, m, bar, x, y, pol);
+    ptx::tma_load_2d(dst + kHalfBytes, m, bar, x + 64, y, pol);
   };
-  const int early = min(2, nb);
+  auto load_k = [&](int j, uint64_t pol) {
+    const uint32_t bar = ctx.bar(kDqKFull + j % kDqKSlots);
+    ptx::mbar_arrive_expect_tx(bar, kTile);
+    load_tile(&p.tmap_k, base + DqSmem::kOffK + (j % kDqKSlots) * kTile, bar, xkv, k0 + kBlockN * j, pol);
+  };
+  auto load_v = [&](int j, uint64_t pol) {
+    const uint32_t bar = ctx.bar(kDqVFull + j % kDqVSlots);
+    ptx::mbar_arrive_expect_tx(bar, kTile);
+    load_tile(&p.tmap_v, base + DqSmem::kOffV + (j % kDqVSlots) * kTile, bar, xkv, k0 + kBlockN * j, pol);
+  };
+  // loads before the set-up sync: K_0, V_0, K_1, V_1, K_2 (every slot once)
+  const int early_k = min(kDqKSlots, nb), early_v = min(kDqVSlots, nb);
 
   if (warp == kWarpProducer && lane == 0) {
     ptx::mbar_init(ctx.bar(kDqQFull), 1);
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(ctx.bar(kDqKVFull + s), 1);
-      ptx::mbar_init(ctx.bar(kDqStageFree + s), 1);
+    for (int s = 0; s < kDqKSlots; ++s) {
+      ptx::mbar_init(ctx.bar(kDqKFull + s), 1);
+      ptx::mbar_init(ctx.bar(kDqKFree + s), 1);
     }
-    ptx::mbar_init(ctx.bar(kDqSReady), 1);
+    for (int s = 0; s < kDqVSlots; ++s) ptx::mbar_init(ctx.bar(kDqVFull + s), 1);
+    ptx::mbar_init(ctx.bar(kDqBlkReady), 1);
+    ptx::mbar_init(ctx.bar(kDqBlkReady + 1), 1);
+    ptx::mbar_init(ctx.bar(kDqDpFree), 4);
     ptx::mbar_init(ctx.bar(kDqPReady), 4);
+    ptx::mbar_init(ctx.bar(kDqPReady + 1), 4);
     ptx::mbar_init(ctx.bar(kDqDone), 1);
     *ctx.abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -160,12 +189,12 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
       const uint64_t pol_kv = ptx::policy_evict_last();
       const uint32_t bar = ctx.bar(kDqQFull);
       ptx::mbar_arrive_expect_tx(bar, 2 * kTile);
-      const int y = q0 + r0;
-      ptx::tma_load_2d(base + DqSmem::kOffQ, &p.tmap_q, bar, xq, y, pol_q);
-      ptx::tma_load_2d(base + DqSmem::kOffQ + kHalfBytes, &p.tmap_q, bar, xq + 64, y, pol_q);
-      ptx::tma_load_2d(base + DqSmem::kOffDo, &p.tmap_do, bar, xq, y, pol_q);
-      ptx::tma_load_2d(base + DqSmem::kOffDo + kHalfBytes, &p.tmap_do, bar, xq + 64, y, pol_q);
-      for (int j = 0; j < early; ++j) load_kv(j, pol_kv);
+      load_tile(&p.tmap_q, base + DqSmem::kOffQ, bar, xq, q0 + r0, pol_q);
+      load_tile(&p.tmap_do, base + DqSmem::kOffDo, bar, xq, q0 + r0, pol_q);
+      for (int j = 0; j < early_k; ++j) {
+        load_k(j, pol_kv);
+        if (j < early_v) load_v(j, pol_kv);
+      }
     }
   }
   if (warp == kWarpMma) {
@@ -212,38 +241,45 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
     const float2 c2 = make_float2(c, c);
     const float2 nl2_2 = make_float2(nl2, nl2);
     const float2 nd2 = make_float2(-dval, -dval);
-    const int key_end = p.causal ? min(row + off + 1, lk) : lk;              // this row's visible keys
-    const int tile_key_end = p.causal ? min(r0 + off + 1, lk) : lk;          // the tile's first row's
+    const int key_end = p.causal ? min(row + off + 1, lk) : lk;      // this row's visible keys
+    const int tile_key_end = p.causal ? min(r0 + off + 1, lk) : lk;  // the tile's first row's
     for (int j = 0; j < nb; ++j) {
-      if (!wait_bar_warp(ctx, kDqSReady, j & 1, kRoleSoftmax)) break;
+      if (!wait_bar_warp(ctx, kDqBlkReady + (j & 1), (j >> 1) & 1, kRoleSoftmax)) break;
       ptx::tc_fence_after();
+      // dP(j) into registers at once, then its columns are released for dP(j+1)
+      float dp[128];
+      ptx::tmem_ld128_wait(lane_base + kDqColDp, dp);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ctx.bar(kDqDpFree));
+      const uint32_t col_s = dq_col_s(j);
       const bool need_mask = tile_key_end - j * kBlockN < kBlockN;  // diagonal or key tail
       const int lim = key_end - j * kBlockN;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        float s[32], dp[32];
-        ptx::tmem_ld32x2_wait(lane_base + kDqColS + 32u * cc, s, lane_base + kDqColDp + 32u * cc, dp);
+        float s[32];
+        ptx::tmem_ld32_wait(lane_base + col_s + 32u * cc, s);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
+          const int kk = 32 * cc + 2 * i;
           const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), c2, nl2_2);
           float p0 = ptx::ex2_approx(x.x);
           float p1 = ptx::ex2_approx(x.y);
           if (need_mask) {
-            const int col = 32 * cc + 2 * i;
-            p0 = col < lim ? p0 : 0.f;
-            p1 = col + 1 < lim ? p1 : 0.f;
+            p0 = kk < lim ? p0 : 0.f;
+            p1 = kk + 1 < lim ? p1 : 0.f;
           }
-          const float2 g = __fadd2_rn(make_float2(dp[2 * i], dp[2 * i + 1]), nd2);  // dP - D
+          const float2 g = __fadd2_rn(make_float2(dp[kk], dp[kk + 1]), nd2);  // dP - D
           const float2 ds = __fmul2_rn(make_float2(p0, p1), g);
           pk[i] = ptx::pack_bf16x2(ds.x, ds.y);
         }
-        ptx::tmem_st16(lane_base + kDqColS + 16u * cc, pk);
+        ptx::tmem_st16(lane_base + col_s + 16u * cc, pk);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ctx.bar(kDqPReady));
+      if (lane == 0) ptx::mbar_arrive(ctx.bar(kDqPReady + (j & 1)));
     }
     // ---- epilogue: dQ * scale -> bf16
     const bool have = nb > 0 && wait_bar_warp(ctx, kDqDone, 0, kRoleSoftmax);
@@ -272,17 +308,33 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
       }
     }
   } else if (warp == kWarpProducer) {
-    // ================================ TMA producer: K/V blocks 2.. through the ring
+    // ================================ TMA producer: the remaining K and V blocks in block order
     if (lane == 0) {
       const uint64_t pol_kv = ptx::policy_evict_last();
-      int issued = early;
-      for (int j = early; j < nb; ++j) {
-        // stage j & 1 last held block j - 2, read by the MMAs of step j - 2
-        if (!wait_bar(ctx, kDqStageFree + (j & 1), ((j >> 1) - 1) & 1, kRoleLoad)) break;
-        load_kv(j, pol_kv);
-        ++issued;
+      int issued_k = early_k, issued_v = early_v;
+      bool ok = true;
+      for (int j = 0; j < nb && ok; ++j) {
+        // K_j reuses the slot of K_(j-3), free once dQ(j-3) retired; V_j the
+        // slot of V_(j-2), free once dP(j-2) retired (its block-ready commit)
+        if (j >= kDqKSlots) {
+          const int prev = j - kDqKSlots;
+          ok = wait_bar(ctx, kDqKFree + prev % kDqKSlots, (prev / kDqKSlots) & 1, kRoleLoad);
+          if (!ok) break;
+          load_k(j, pol_kv);
+          ++issued_k;
+        }
+        if (j >= kDqVSlots) {
+          const int prev = j - kDqVSlots;
+          ok = wait_bar(ctx, kDqBlkReady + (prev & 1), (prev >> 1) & 1, kRoleLoad);
+          if (!ok) break;
+          load_v(j, pol_kv);
+          ++issued_v;
+        }
       }
-      for (int j = max(0, issued - 2); j < issued; ++j) wait_drain(ctx, kDqKVFull + (j & 1), (j >> 1) & 1);
+      for (int j = max(0, issued_k - kDqKSlots); j < issued_k; ++j)
+        wait_drain(ctx, kDqKFull + j % kDqKSlots, (j / kDqKSlots) & 1);
+      for (int j = max(0, issued_v - kDqVSlots); j < issued_v; ++j)
+        wait_drain(ctx, kDqVFull + j % kDqVSlots, (j / kDqVSlots) & 1);
       if (nb > 0) wait_drain(ctx, kDqQFull, 0);
     }
     __syncwarp();
@@ -291,32 +343,47 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
     if (lane == 0 && nb > 0) {
       const uint64_t q_desc = desc_kmajor(base + DqSmem::kOffQ);
       const uint64_t do_desc = desc_kmajor(base + DqSmem::kOffDo);
-      const uint64_t ring_kmaj = desc_kmajor(base + DqSmem::kOffRing);
-      const uint64_t ring_mn = desc_mnmajor(base + DqSmem::kOffRing);
+      const uint64_t k_kmaj = desc_kmajor(base + DqSmem::kOffK);
+      const uint64_t k_mn = desc_mnmajor(base + DqSmem::kOffK);
+      const uint64_t v_kmaj = desc_kmajor(base + DqSmem::kOffV);
       constexpr uint64_t kStep = kTile >> 4;  // descriptor units of one tile
+      auto wait_k = [&](int j) { return wait_bar(ctx, kDqKFull + j % kDqKSlots, (j / kDqKSlots) & 1, kRoleMma); };
+      auto wait_v = [&](int j) { return wait_bar(ctx, kDqVFull + j % kDqVSlots, (j / kDqVSlots) & 1, kRoleMma); };
+      auto issue_s = [&](int j) { issue_qk<128>(tmem + dq_col_s(j), q_desc, k_kmaj + (j % kDqKSlots) * kStep); };
+      auto issue_dp = [&](int j) { issue_qk<128>(tmem + kDqColDp, do_desc, v_kmaj + (j % kDqVSlots) * kStep); };
       bool issued_any = false;
-      bool ok = wait_bar(ctx, kDqQFull, 0, kRoleMma) && wait_bar(ctx, kDqKVFull, 0, kRoleMma);
+      bool ok = wait_bar(ctx, kDqQFull, 0, kRoleMma) && wait_k(0) && wait_v(0);
       if (ok) {
         ptx::tc_fence_after();
-        issue_qk<128>(tmem + kDqColS, q_desc, ring_kmaj);               // S(0) = Q K_0^T
-        issue_qk<128>(tmem + kDqColDp, do_desc, ring_kmaj + kStep);     // dP(0) = dO V_0^T
-        ptx::mma_commit(ctx.bar(kDqSReady));
+        issue_s(0);
+        issue_dp(0);
+        ptx::mma_commit(ctx.bar(kDqBlkReady));  // block 0
         issued_any = true;
+        if (nb > 1) {
+          ok = wait_k(1);
+          if (ok) {
+            ptx::tc_fence_after();
+            issue_s(1);
+          }
+        }
       }
       for (int j = 0; j < nb && ok; ++j) {
-        const int s = j & 1;
-        if (!wait_bar(ctx, kDqPReady, j & 1, kRoleMma)) break;
-        ptx::tc_fence_after();
-        // dQ += dS(j) K_j: A = dS (bf16 over S), B = K_j MN-major
-        issue_pv<128>(tmem + kDqColDq, tmem + kDqColS, ring_mn + 2 * s * kStep, j > 0);
-        ptx::mma_commit(ctx.bar(kDqStageFree + s));
         if (j + 1 < nb) {
-          const int s1 = (j + 1) & 1;
-          if (!wait_bar(ctx, kDqKVFull + s1, ((j + 1) >> 1) & 1, kRoleMma)) break;
+          // dP(j) is in the gradient warps' registers: dP(j+1) into its columns
+          if (!wait_bar(ctx, kDqDpFree, j & 1, kRoleMma) || !wait_v(j + 1)) break;
           ptx::tc_fence_after();
-          issue_qk<128>(tmem + kDqColS, q_desc, ring_kmaj + 2 * s1 * kStep);
-          issue_qk<128>(tmem + kDqColDp, do_desc, ring_kmaj + (2 * s1 + 1) * kStep);
-          ptx::mma_commit(ctx.bar(kDqSReady));
+          issue_dp(j + 1);
+          ptx::mma_commit(ctx.bar(kDqBlkReady + ((j + 1) & 1)));  // block j+1: S(j+1) was issued earlier
+        }
+        if (!wait_bar(ctx, kDqPReady + (j & 1), (j >> 1) & 1, kRoleMma)) break;
+        ptx::tc_fence_after();
+        // dQ += dS(j) K_j: A = dS (bf16 over S(j)), B = K_j MN-major
+        issue_pv<128>(tmem + kDqColDq, tmem + dq_col_s(j), k_mn + (j % kDqKSlots) * kStep, j > 0);
+        ptx::mma_commit(ctx.bar(kDqKFree + j % kDqKSlots));
+        if (j + 2 < nb) {
+          if (!wait_k(j + 2)) break;
+          ptx::tc_fence_after();
+          issue_s(j + 2);  // into the S buffer dQ(j) has just read (in order)
         }
       }
       if (issued_any) {
@@ -350,10 +417,40 @@ struct DkvSmem {
 constexpr int kKvKVFull = 0;      // K, V landed
 constexpr int kKvStageFull = 1;   // [2] Q, dO and the row terms of stage s
 constexpr int kKvStageFree = 3;   // [2] the MMAs reading stage s retired
-constexpr int kKvSReady = 5;      // S^T, dP^T in TMEM
-constexpr int kKvPReady = 6;      // P^T, dS^T stored (4 warps)
-constexpr int kKvDone = 7;        // every MMA retired
-constexpr uint32_t kKvColS = 0, kKvColDp = 128, kKvColDv = 256, kKvColDk = 384;
+constexpr int kKvHalfReady = 5;   // [2] S^T, dP^T of query half h in TMEM
+constexpr int kKvPReady = 7;      // [2] P^T, dS^T of query half h stored (4 warps)
+constexpr int kKvDone = 9;        // every MMA retired
+// TMEM columns.  Each 128-query block is processed as two halves of 64
+// queries: S^T of half h at 64 h, dP^T at 128 + 64 h (P^T and dS^T as bf16
+// over their first 32 columns), dV at 256, dK at 384.
+constexpr uint32_t kKvColDp = 128, kKvColDv = 256, kKvColDk = 384;
+constexpr uint32_t kQHalfBytes = 64 * 128;  // 64 rows of a swizzled 64-column half
+
+// S^T_h = K Q_h^T (or dP^T_h = V dO_h^T): M=128 keys, N=64 queries (rows
+// 64 h .. 64 h + 63 of the Q tile, 8 KiB into each swizzled half), K=128 head
+// dims in 8 steps.
+__device__ __forceinline__ void issue_half_qk(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc) {
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, 64, false, false);
+  ptx::mma_ss_imm<false>(tmem_d, a_desc, b_desc, idesc);
+#pragma unroll
+  for (int k = 1; k < 8; ++k) {
+    const uint64_t off = ((k >> 2) * kHalfBytes + (k & 3) * 32u) >> 4;
+    ptx::mma_ss_imm<true>(tmem_d, a_desc + off, b_desc + off, idesc);
+  }
+}
+
+// dV += P^T_h dO_h (or dK += dS^T_h Q_h): M=128 keys, N=128 head dims, K=64
+// queries in 4 steps; A from TMEM (8 columns per step), B MN-major from the
+// rows of half h.
+__device__ __forceinline__ void issue_half_pv(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc, bool accumulate) {
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, 128, false, true);
+  if (accumulate)
+    ptx::mma_ts_imm<true>(tmem_d, tmem_a, b_desc, idesc);
+  else
+    ptx::mma_ts_imm<false>(tmem_d, tmem_a, b_desc, idesc);
+#pragma unroll
+  for (int k = 1; k < 4; ++k) ptx::mma_ts_imm<true>(tmem_d, tmem_a + 8u * k, b_desc + ((2048u * k) >> 4), idesc);
+}
 
 __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -393,9 +490,9 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(ctx.bar(kKvStageFull + s), 1);
       ptx::mbar_init(ctx.bar(kKvStageFree + s), 1);
+      ptx::mbar_init(ctx.bar(kKvHalfReady + s), 1);
+      ptx::mbar_init(ctx.bar(kKvPReady + s), 4);
     }
-    ptx::mbar_init(ctx.bar(kKvSReady), 1);
-    ptx::mbar_init(ctx.bar(kKvPReady), 4);
     ptx::mbar_init(ctx.bar(kKvDone), 1);
     *ctx.abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -426,46 +523,54 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid
     const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp) * 32u) << 16);
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
-    for (int it = 0; it < n_items; ++it) {
+    bool ok = true;
+    for (int it = 0; it < n_items && ok; ++it) {
       const int s = it & 1;
       const int m = m_start + it % nm;
-      // the row terms of this stage (written by the producer's threads) and S^T, dP^T
+      // the row terms of this stage (written by the producer's threads)
       if (!wait_bar_warp(ctx, kKvStageFull + s, (it >> 1) & 1, kRoleSoftmax)) break;
-      if (!wait_bar_warp(ctx, kKvSReady, it & 1, kRoleSoftmax)) break;
-      ptx::tc_fence_after();
       // causal: key jr is visible to query column cq iff jr <= m * 128 + cq + off
       const bool need_mask = p.causal && (m * kBlockM + off < j0 + kBlockN - 1);
       const int cmin = jr - off - m * kBlockM;  // first visible column
       const uint32_t rowterms = base + DkvSmem::kOffRow + 1024u * s;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float st[32], dpt[32];
-        ptx::tmem_ld32x2_wait(lane_base + kKvColS + 32u * cc, st, lane_base + kKvColDp + 32u * cc, dpt);
-        uint32_t pk[16], dk16[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int col = 32 * cc + 2 * i;
-          const float2 nl = ptx::ld_shared_v2f(rowterms + 4u * col);
-          const float2 nd = ptx::ld_shared_v2f(rowterms + 512u + 4u * col);
-          const float2 x = __ffma2_rn(make_float2(st[2 * i], st[2 * i + 1]), c2, nl);
-          float p0 = ptx::ex2_approx(x.x);
-          float p1 = ptx::ex2_approx(x.y);
-          if (need_mask) {
-            p0 = col >= cmin ? p0 : 0.f;
-            p1 = col + 1 >= cmin ? p1 : 0.f;
-          }
-          const float2 g = __fadd2_rn(make_float2(dpt[2 * i], dpt[2 * i + 1]), nd);  // dP - D
-          const float2 ds = __fmul2_rn(make_float2(p0, p1), g);
-          pk[i] = ptx::pack_bf16x2(p0, p1);
-          dk16[i] = ptx::pack_bf16x2(ds.x, ds.y);
+      for (int hf = 0; hf < 2; ++hf) {
+        if (!wait_bar_warp(ctx, kKvHalfReady + hf, it & 1, kRoleSoftmax)) {
+          ok = false;
+          break;
         }
-        ptx::tmem_st16(lane_base + kKvColS + 16u * cc, pk);
-        ptx::tmem_st16(lane_base + kKvColDp + 16u * cc, dk16);
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          float st[32], dpt[32];
+          ptx::tmem_ld32x2_wait(lane_base + 64u * hf + 32u * cc, st, lane_base + kKvColDp + 64u * hf + 32u * cc,
+                                dpt);
+          uint32_t pk[16], dk16[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int col = 64 * hf + 32 * cc + 2 * i;
+            const float2 nl = ptx::ld_shared_v2f(rowterms + 4u * col);
+            const float2 nd = ptx::ld_shared_v2f(rowterms + 512u + 4u * col);
+            const float2 x = __ffma2_rn(make_float2(st[2 * i], st[2 * i + 1]), c2, nl);
+            float p0 = ptx::ex2_approx(x.x);
+            float p1 = ptx::ex2_approx(x.y);
+            if (need_mask) {
+              p0 = col >= cmin ? p0 : 0.f;
+              p1 = col + 1 >= cmin ? p1 : 0.f;
+            }
+            const float2 g = __fadd2_rn(make_float2(dpt[2 * i], dpt[2 * i + 1]), nd);  // dP - D
+            const float2 ds = __fmul2_rn(make_float2(p0, p1), g);
+            pk[i] = ptx::pack_bf16x2(p0, p1);
+            dk16[i] = ptx::pack_bf16x2(ds.x, ds.y);
+          }
+          ptx::tmem_st16(lane_base + 64u * hf + 16u * cc, pk);
+          ptx::tmem_st16(lane_base + kKvColDp + 64u * hf + 16u * cc, dk16);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ctx.bar(kKvPReady + hf));
       }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ctx.bar(kKvPReady));
     }
     // ---- epilogue: dV, dK * scale -> bf16 (keys of the sequence only)
     const bool have = n_items > 0 && wait_bar_warp(ctx, kKvDone, 0, kRoleSoftmax);
@@ -549,35 +654,56 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid
     __syncwarp();
   } else {
     // ================================ MMA issuer
+    // Per item (query block), per half h of 64 queries: dV/dK of item it, half
+    // h, as soon as its P^T/dS^T are stored, then S^T/dP^T of item it + 1,
+    // half h into the columns those products just read.  The gradient math of
+    // one half overlaps the tensor work of the other.
     if (lane == 0 && n_items > 0) {
       const uint64_t k_desc = desc_kmajor(base + DkvSmem::kOffK);
       const uint64_t v_desc = desc_kmajor(base + DkvSmem::kOffV);
-      const uint64_t ring_kmaj = desc_kmajor(base + DkvSmem::kOffRing);
-      const uint64_t ring_mn = desc_mnmajor(base + DkvSmem::kOffRing);
       constexpr uint64_t kStep = kTile >> 4;
+      constexpr uint64_t kHalfRows = kQHalfBytes >> 4;  // rows 64.. of a tile, in descriptor units
+      auto q_tile = [&](int it) { return base + DkvSmem::kOffRing + 2u * (it & 1) * kTile; };
+      auto issue_scores = [&](int it, int hf) {
+        const uint64_t q_kmaj = desc_kmajor(q_tile(it)) + hf * kHalfRows;
+        const uint64_t do_kmaj = desc_kmajor(q_tile(it) + kTile) + hf * kHalfRows;
+        issue_half_qk(tmem + 64u * hf, k_desc, q_kmaj);             // S^T_h = K Q_h^T
+        issue_half_qk(tmem + kKvColDp + 64u * hf, v_desc, do_kmaj);  // dP^T_h = V dO_h^T
+        ptx::mma_commit(ctx.bar(kKvHalfReady + hf));
+      };
       bool issued_any = false;
       bool ok = wait_bar(ctx, kKvKVFull, 0, kRoleMma) && wait_bar(ctx, kKvStageFull, 0, kRoleMma);
       if (ok) {
         ptx::tc_fence_after();
-        issue_qk<128>(tmem + kKvColS, k_desc, ring_kmaj);            // S^T(0) = K Q_0^T
-        issue_qk<128>(tmem + kKvColDp, v_desc, ring_kmaj + kStep);   // dP^T(0) = V dO_0^T
-        ptx::mma_commit(ctx.bar(kKvSReady));
+        issue_scores(0, 0);
+        issue_scores(0, 1);
         issued_any = true;
       }
       for (int it = 0; it < n_items && ok; ++it) {
         const int s = it & 1;
-        if (!wait_bar(ctx, kKvPReady, it & 1, kRoleMma)) break;
-        ptx::tc_fence_after();
-        issue_pv<128>(tmem + kKvColDv, tmem + kKvColS, ring_mn + (2 * s + 1) * kStep, it > 0);  // dV += P^T dO
-        issue_pv<128>(tmem + kKvColDk, tmem + kKvColDp, ring_mn + 2 * s * kStep, it > 0);       // dK += dS^T Q
-        ptx::mma_commit(ctx.bar(kKvStageFree + s));
-        if (it + 1 < n_items) {
-          const int s1 = (it + 1) & 1;
-          if (!wait_bar(ctx, kKvStageFull + s1, ((it + 1) >> 1) & 1, kRoleMma)) break;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!wait_bar(ctx, kKvPReady + hf, it & 1, kRoleMma)) {
+            ok = false;
+            break;
+          }
           ptx::tc_fence_after();
-          issue_qk<128>(tmem + kKvColS, k_desc, ring_kmaj + 2 * s1 * kStep);
-          issue_qk<128>(tmem + kKvColDp, v_desc, ring_kmaj + (2 * s1 + 1) * kStep);
-          ptx::mma_commit(ctx.bar(kKvSReady));
+          const bool acc = it > 0 || hf > 0;
+          const uint64_t q_mn = desc_mnmajor(q_tile(it)) + hf * kHalfRows;
+          const uint64_t do_mn = desc_mnmajor(q_tile(it) + kTile) + hf * kHalfRows;
+          issue_half_pv(tmem + kKvColDv, tmem + 64u * hf, do_mn, acc);             // dV += P^T_h dO_h
+          issue_half_pv(tmem + kKvColDk, tmem + kKvColDp + 64u * hf, q_mn, acc);   // dK += dS^T_h Q_h
+          if (hf == 1) ptx::mma_commit(ctx.bar(kKvStageFree + s));
+          if (it + 1 < n_items) {
+            if (hf == 0) {
+              if (!wait_bar(ctx, kKvStageFull + ((it + 1) & 1), ((it + 1) >> 1) & 1, kRoleMma)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+            }
+            issue_scores(it + 1, hf);
+          }
         }
       }
       if (issued_any) {
