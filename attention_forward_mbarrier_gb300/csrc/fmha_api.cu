@@ -364,7 +364,13 @@ extern "C" int fmha_bwd(const void* q, const void* k, const void* v, const void*
 
   if (configure_bwd() != 0) return FMHA_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // dQ (and D = rowsum(dO * O) into the workspace) first, then dK / dV, which read D
+  // D = rowsum(dO * O) into the workspace, then dQ, then dK / dV (both read D)
+  if (total_q > 0) {
+    const int64_t rows = static_cast<int64_t>(total_q) * heads;
+    const int64_t blocks = std::min<int64_t>((rows + 15) / 16, 152 * 32);  // 16 rows per 256-thread block pass
+    fmha::bwd::fmha_bwd_dot_kernel<<<static_cast<unsigned>(blocks), fmha::bwd::kDotThreads, 0, st>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
+  }
   if (qblocks > 0 && total_q > 0) {
     fmha::bwd::fmha_bwd_dq_kernel<<<dim3(heads, qblocks, batch), fmha::bwd::kThreads, fmha::bwd::DqSmem::kBytes,
                                     st>>>(p);
@@ -464,6 +470,15 @@ extern "C" int fmha_version(void) { return 10100; }
 extern "C" int fmha_debug_set_trace(void* device_buffer) {
   unsigned long long* p = static_cast<unsigned long long*>(device_buffer);
   return cudaMemcpyToSymbol(fmha::g_trace, &p, sizeof(p)) == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
+}
+
+// Trace builds only: backward-pass stamps, (query blocks) x 1024 and (key
+// blocks) x 1024 uint64 slots for the dQ and dK/dV kernels, or nullptr.
+extern "C" int fmha_debug_set_bwd_trace(void* dq_buffer, void* dkdv_buffer) {
+  unsigned long long* a = static_cast<unsigned long long*>(dq_buffer);
+  unsigned long long* b = static_cast<unsigned long long*>(dkdv_buffer);
+  if (cudaMemcpyToSymbol(fmha::bwd::g_trace_dq, &a, sizeof(a)) != cudaSuccess) return FMHA_ERR_CUDA;
+  return cudaMemcpyToSymbol(fmha::bwd::g_trace_dkdv, &b, sizeof(b)) == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
 }
 
 // Trace builds only: per-CTA table of 4 uint64 per CTA (grid size x 4), or nullptr.

@@ -11,10 +11,11 @@
 //   dV = P^T dO,  dP = dO V^T,  D_i = dO_i . O_i,  dS = P * (dP - D),
 //   dQ = scale * dS K,  dK = scale * dS^T Q.
 //
-// Two kernels, no atomics (every output row is written by one CTA):
-//   fmha_bwd_dq_kernel    one CTA per (head, 128 query rows, sequence): first
-//                         D_i (written to the workspace for the second kernel),
-//                         then per 128-key block S = Q K^T and dP = dO V^T into
+// Three kernels, no atomics (every output row is written by one CTA):
+//   fmha_bwd_dot_kernel   D_i = dO_i . O_i for every row, into the workspace
+//                         (coalesced, bandwidth-bound);
+//   fmha_bwd_dq_kernel    one CTA per (head, 128 query rows, sequence): per
+//                         128-key block S = Q K^T and dP = dO V^T into
 //                         TMEM, dS in bf16 over S, dQ += dS K; S is
 //                         double-buffered and dP released as soon as it is in
 //                         registers, so the next blocks' products overlap the
@@ -63,6 +64,23 @@ struct alignas(64) BwdParams {
   float scale_log2;  // scale * log2(e)
 };
 
+// Opt-in coarse trace (build with -DFMHA_TRACE): %clock64 stamps of the CTAs
+// of head (K/V head) 0, sequence 0, one row of kTraceSlots per query (key)
+// block: per block / item j < 64 at slot 8 j + event, set-up and exit at
+// 1000 + event.
+#ifdef FMHA_TRACE
+__device__ unsigned long long* g_trace_dq;
+__device__ unsigned long long* g_trace_dkdv;
+#define FMHA_BWD_TRACE(row, slot)                                                            \
+  do {                                                                                       \
+    if ((row) != nullptr) (row)[(slot)] = static_cast<unsigned long long>(clock64());       \
+  } while (0)
+#else
+#define FMHA_BWD_TRACE(row, slot) \
+  do {                            \
+  } while (0)
+#endif
+
 __device__ __forceinline__ void seq_bounds(const BwdParams& p, int b, int& q0, int& lq, int& k0, int& lk) {
   if (p.cu_q != nullptr) {
     q0 = p.cu_q[b];
@@ -83,6 +101,43 @@ __device__ __forceinline__ void seq_bounds(const BwdParams& p, int b, int& q0, i
 // row with no visible key (LSE = -inf), whose P must be 0 (its keys are all
 // masked anyway).
 __device__ __forceinline__ float neg_lse2(float lse) { return lse == -INFINITY ? -INFINITY : -lse * kLog2e; }
+
+// ============================================================================ D
+// D_i = dO_i . O_i (fp32) for every (token, head) row, into the workspace
+// [heads, total_q].  Coalesced: 16 lanes per 256-byte row, two rows per warp
+// instruction, grid-stride over the rows.  (Rows of no sequence get a value
+// that nothing reads.)
+constexpr int kDotThreads = 256;
+__global__ void __launch_bounds__(kDotThreads) fmha_bwd_dot_kernel(const __grid_constant__ BwdParams p) {
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4, sub = lane & 15;
+  const int64_t rows = static_cast<int64_t>(p.total_q) * p.heads;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t r2 = warp0; 2 * r2 < rows; r2 += nwarps) {
+    const int64_t r = 2 * r2 + half;  // row = token * heads + head
+    float acc = 0.f;
+    if (r < rows) {
+      const uint4 a = *reinterpret_cast<const uint4*>(p.out + r * 128 + 8 * sub);
+      const uint4 g = *reinterpret_cast<const uint4*>(p.dout + r * 128 + 8 * sub);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[k]));
+        const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv[k]));
+        acc = fmaf(af.x, gf.x, acc);
+        acc = fmaf(af.y, gf.y, acc);
+      }
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);  // within each 16-lane half
+    if (sub == 0 && r < rows) {
+      const int64_t tok = r / p.heads;
+      const int h = static_cast<int>(r - tok * p.heads);
+      p.dvec[static_cast<int64_t>(h) * p.total_q + tok] = acc;
+    }
+  }
+}
 
 // ============================================================================ dQ
 // Shared memory: Q and dO tiles, a 3-slot ring of K blocks and a 2-slot ring
@@ -145,6 +200,12 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
   const int off = lk - lq;
   const int nb = tile_blocks(r0, lq, lk, p.causal);
   const int xq = h * 128;
+#ifdef FMHA_TRACE
+  unsigned long long* trow = (g_trace_dq != nullptr && h == 0 && b == 0) ? g_trace_dq + blockIdx.y * 1024ull : nullptr;
+#else
+  unsigned long long* trow = nullptr;
+#endif
+  if (threadIdx.x == 0) FMHA_BWD_TRACE(trow, 1000);
   const int xkv = (h / p.kv_group) * 128;
 
   Ctx ctx;
@@ -215,26 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
     float dval = 0.f;
     float nl2 = -INFINITY;  // rows past the sequence end: P = 0
     if (valid) {
-      // D_i = dO_i . O_i (fp32), also kept for the dK/dV kernel
-      const size_t e = (static_cast<size_t>(q0 + row) * p.heads + h) * 128;
-      const uint4* o4 = reinterpret_cast<const uint4*>(p.out + e);
-      const uint4* g4 = reinterpret_cast<const uint4*>(p.dout + e);
-      float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const uint4 a = o4[i], g = g4[i];
-        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[k]));
-          const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv[k]));
-          acc0 = fmaf(af.x, gf.x, acc0);
-          acc1 = fmaf(af.y, gf.y, acc1);
-        }
-      }
-      dval = acc0 + acc1;
+      // D_i (from the pre-pass) and the row's LSE
       const size_t li = static_cast<size_t>(h) * p.total_q + q0 + row;
-      p.dvec[li] = dval;
+      dval = p.dvec[li];
       nl2 = neg_lse2(p.lse[li]);
     }
     const float c = p.scale_log2;
@@ -243,8 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
     const float2 nd2 = make_float2(-dval, -dval);
     const int key_end = p.causal ? min(row + off + 1, lk) : lk;      // this row's visible keys
     const int tile_key_end = p.causal ? min(r0 + off + 1, lk) : lk;  // the tile's first row's
+    const bool tr = r == 0 && trow != nullptr;
+    if (tr) FMHA_BWD_TRACE(trow, 1001);
     for (int j = 0; j < nb; ++j) {
       if (!wait_bar_warp(ctx, kDqBlkReady + (j & 1), (j >> 1) & 1, kRoleSoftmax)) break;
+      if (tr && j < 64) FMHA_BWD_TRACE(trow, 8 * j + 0);
       ptx::tc_fence_after();
       // dP(j) into registers at once, then its columns are released for dP(j+1)
       float dp[128];
@@ -252,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ctx.bar(kDqDpFree));
+      if (tr && j < 64) FMHA_BWD_TRACE(trow, 8 * j + 1);
       const uint32_t col_s = dq_col_s(j);
       const bool need_mask = tile_key_end - j * kBlockN < kBlockN;  // diagonal or key tail
       const int lim = key_end - j * kBlockN;
@@ -280,7 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ctx.bar(kDqPReady + (j & 1)));
+      if (tr && j < 64) FMHA_BWD_TRACE(trow, 8 * j + 2);
     }
+    if (tr) FMHA_BWD_TRACE(trow, 1002);
     // ---- epilogue: dQ * scale -> bf16
     const bool have = nb > 0 && wait_bar_warp(ctx, kDqDone, 0, kRoleSoftmax);
     if (have) ptx::tc_fence_after();
@@ -370,18 +420,23 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
       for (int j = 0; j < nb && ok; ++j) {
         if (j + 1 < nb) {
           // dP(j) is in the gradient warps' registers: dP(j+1) into its columns
-          if (!wait_bar(ctx, kDqDpFree, j & 1, kRoleMma) || !wait_v(j + 1)) break;
+          if (!wait_bar(ctx, kDqDpFree, j & 1, kRoleMma)) break;
+          if (j < 64) FMHA_BWD_TRACE(trow, 8 * j + 3);
+          if (!wait_v(j + 1)) break;
+          if (j < 64) FMHA_BWD_TRACE(trow, 8 * j + 6);
           ptx::tc_fence_after();
           issue_dp(j + 1);
           ptx::mma_commit(ctx.bar(kDqBlkReady + ((j + 1) & 1)));  // block j+1: S(j+1) was issued earlier
         }
         if (!wait_bar(ctx, kDqPReady + (j & 1), (j >> 1) & 1, kRoleMma)) break;
+        if (j < 64) FMHA_BWD_TRACE(trow, 8 * j + 4);
         ptx::tc_fence_after();
         // dQ += dS(j) K_j: A = dS (bf16 over S(j)), B = K_j MN-major
         issue_pv<128>(tmem + kDqColDq, tmem + dq_col_s(j), k_mn + (j % kDqKSlots) * kStep, j > 0);
         ptx::mma_commit(ctx.bar(kDqKFree + j % kDqKSlots));
         if (j + 2 < nb) {
           if (!wait_k(j + 2)) break;
+          if (j < 64) FMHA_BWD_TRACE(trow, 8 * j + 5);
           ptx::tc_fence_after();
           issue_s(j + 2);  // into the S buffer dQ(j) has just read (in order)
         }
@@ -472,6 +527,13 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid
   seq_bounds(p, b, q0, lq, k0, lk);
   if (j0 >= lk) return;
   const int off = lk - lq;
+#ifdef FMHA_TRACE
+  unsigned long long* trow =
+      (g_trace_dkdv != nullptr && hk == 0 && b == 0) ? g_trace_dkdv + blockIdx.y * 1024ull : nullptr;
+#else
+  unsigned long long* trow = nullptr;
+#endif
+  if (threadIdx.x == 0) FMHA_BWD_TRACE(trow, 1000);
   // query blocks that see some key of this block: causal rows i see keys j <= i + off
   const int m_end = (lq + kBlockM - 1) / kBlockM;
   const int m_start = p.causal ? max(0, j0 - off) / kBlockM : 0;
@@ -523,12 +585,15 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid
     const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp) * 32u) << 16);
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
+    const bool tr = r == 0 && trow != nullptr;
+    if (tr) FMHA_BWD_TRACE(trow, 1001);
     bool ok = true;
     for (int it = 0; it < n_items && ok; ++it) {
       const int s = it & 1;
       const int m = m_start + it % nm;
       // the row terms of this stage (written by the producer's threads)
       if (!wait_bar_warp(ctx, kKvStageFull + s, (it >> 1) & 1, kRoleSoftmax)) break;
+      if (tr && it < 64) FMHA_BWD_TRACE(trow, 8 * it + 0);
       // causal: key jr is visible to query column cq iff jr <= m * 128 + cq + off
       const bool need_mask = p.causal && (m * kBlockM + off < j0 + kBlockN - 1);
       const int cmin = jr - off - m * kBlockM;  // first visible column
@@ -539,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid
           ok = false;
           break;
         }
+        if (tr && it < 64) FMHA_BWD_TRACE(trow, 8 * it + 1 + 2 * hf);
         ptx::tc_fence_after();
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -570,8 +636,10 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ctx.bar(kKvPReady + hf));
+        if (tr && it < 64) FMHA_BWD_TRACE(trow, 8 * it + 2 + 2 * hf);
       }
     }
+    if (tr) FMHA_BWD_TRACE(trow, 1002);
     // ---- epilogue: dV, dK * scale -> bf16 (keys of the sequence only)
     const bool have = n_items > 0 && wait_bar_warp(ctx, kKvDone, 0, kRoleSoftmax);
     if (have) ptx::tc_fence_after();
@@ -614,11 +682,9 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid
       const int s = it & 1;
       const int h = hk * group + it / nm;
       const int m = m_start + it % nm;
-      if (it >= 2) ok = wait_bar_warp(ctx, kKvStageFree + s, ((it >> 1) - 1) & 1, kRoleLoad);
-      if (!ok) break;
       // row terms: -LSE log2(e) and -D of the block's 128 query rows (rows
-      // past the sequence end get -inf, so their P is 0)
-      const uint32_t rowterms = base + DkvSmem::kOffRow + 1024u * s;
+      // past the sequence end get -inf, so their P is 0), read from global
+      // memory before waiting for the stage so that the wait hides them
       float nl[4], dd[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -631,6 +697,10 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid
           dd[i] = -p.dvec[li];
         }
       }
+      if (it >= 2) ok = wait_bar_warp(ctx, kKvStageFree + s, ((it >> 1) - 1) & 1, kRoleLoad);
+      if (!ok) break;
+      if (lane == 0 && it < 64) FMHA_BWD_TRACE(trow, 8 * it + 7);
+      const uint32_t rowterms = base + DkvSmem::kOffRow + 1024u * s;
       ptx::st_shared_v4f(rowterms + 16u * lane, nl[0], nl[1], nl[2], nl[3]);
       ptx::st_shared_v4f(rowterms + 512u + 16u * lane, dd[0], dd[1], dd[2], dd[3]);
       __syncwarp();
@@ -687,6 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid
             ok = false;
             break;
           }
+          if (it < 64) FMHA_BWD_TRACE(trow, 8 * it + 5 + hf);
           ptx::tc_fence_after();
           const bool acc = it > 0 || hf > 0;
           const uint64_t q_mn = desc_mnmajor(q_tile(it)) + hf * kHalfRows;

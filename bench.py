@@ -399,7 +399,7 @@ def backward_only(w: wl.Workload, dev, peak: float, steps: int = 5, warmup: int 
     del q, k, v, g, out, lse, dq, dk, dv, ws, flusher
     torch.cuda.empty_cache()
     return {"tflops": tf, "frac_of_peak": tf / peak, "ms": bwd_ms, "gflop": flops / 1e9, "causal": w.causal,
-            "launches": 2, "fwd_bwd_ms": step_ms,
+            "launches": 3, "fwd_bwd_ms": step_ms,
             "fwd_bwd_tflops": 3.5 * w.flops() / (step_ms * 1e-3) / 1e12}
 
 

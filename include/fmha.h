@@ -178,7 +178,7 @@ size_t fmha_fwd_fp8pv_workspace_size(int batch, int total_k, int kv_heads, int h
  * Every 16-byte alignment rule of fmha_fwd applies to q, k, v, out, dout,
  * dq, dk and dv.
  *
- * Two kernels are enqueued on `stream` (dQ and D first, then dK and dV); the
+ * Three kernels are enqueued on `stream` (D, then dQ, then dK and dV); the
  * call allocates nothing and never synchronises.  Returns as fmha_fwd does.
  */
 int fmha_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout,

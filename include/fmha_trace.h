@@ -29,6 +29,14 @@ int fmha_debug_set_trace(void *device_buffer);
  */
 int fmha_debug_set_cta_trace(void *device_buffer);
 
+/*
+ * fmha_debug_set_bwd_trace -- caller-owned device buffers of
+ * ceil(max_seqlen_q / 128) x 1024 and ceil(max_seqlen_k / 128) x 1024 uint64
+ * for the %clock64 stamps of the backward pass's dQ and dK/dV kernels (CTAs
+ * of head 0, sequence 0), or NULL to stop.
+ */
+int fmha_debug_set_bwd_trace(void *dq_buffer, void *dkdv_buffer);
+
 #ifdef __cplusplus
 }
 #endif
