@@ -254,10 +254,9 @@ extern "C" int fmha_fwd_fp8pv(const void* q, const void* k, const void* v, void*
   pp.head_dim = head_dim;
   pp.kpad = kpad;
   if (cudaMemsetAsync(amax, 0, static_cast<size_t>(kv_heads) * 4, st) != cudaSuccess) return FMHA_ERR_CUDA;
-  const int64_t rows = static_cast<int64_t>(total_k) * kv_heads;
-  if (rows > 0) {
-    const int64_t blocks = std::min<int64_t>((rows + 7) / 8, 152 * 16);
-    fmha::fp8::v_amax_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(pp);
+  if (total_k > 0) {
+    const int64_t chunks = (static_cast<int64_t>(total_k) + fmha::fp8::kAmaxTokens - 1) / fmha::fp8::kAmaxTokens;
+    fmha::fp8::v_amax_kernel<<<dim3(static_cast<unsigned>(chunks), kv_heads), fmha::fp8::kAmaxThreads, 0, st>>>(pp);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
   }
   if (kpad > 0) {

@@ -41,20 +41,38 @@ __device__ __forceinline__ int64_t seq_key_start(const PrepassParams& p, int b) 
   return p.cu_k != nullptr ? static_cast<int64_t>(p.cu_k[b]) : static_cast<int64_t>(b) * p.max_seqlen_k;
 }
 
-// max |V| per K/V head: grid-stride over (token, head) rows, one warp per row.
-__global__ void __launch_bounds__(256) v_amax_kernel(const PrepassParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t rows = static_cast<int64_t>(p.total_k) * p.kv_heads;
-  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t r = warp0; r < rows; r += nwarps) {
-    const int h = static_cast<int>(r % p.kv_heads);
-    const __nv_bfloat16* row = p.v + r * p.head_dim;
-    float m = 0.f;
-    for (int d = lane; d < p.head_dim; d += 32) m = fmaxf(m, fabsf(__bfloat162float(row[d])));
+// max |V| per K/V head: one CTA per (token chunk, K/V head); each warp takes
+// tokens of the chunk (16 lanes per 256-byte row, two rows per instruction),
+// the CTA reduces in shared memory and makes one atomicMax (non-negative
+// floats order as their bits), so the atomics stay few per head.
+constexpr int kAmaxThreads = 256;
+constexpr int kAmaxTokens = 64;  // tokens per CTA (many CTAs: the pass is latency-bound)
+__global__ void __launch_bounds__(kAmaxThreads) v_amax_kernel(const PrepassParams p) {
+  __shared__ float warp_max[kAmaxThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int half = lane >> 4, sub = lane & 15;
+  const int h = static_cast<int>(blockIdx.y);
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kAmaxTokens;
+  const int64_t t1 = min(t0 + kAmaxTokens, static_cast<int64_t>(p.total_k));
+  float m = 0.f;
+  for (int64_t t = t0 + 2 * warp + half; t < t1; t += 2 * (kAmaxThreads / 32)) {
+    const uint4 v4 = *reinterpret_cast<const uint4*>(p.v + (t * p.kv_heads + h) * p.head_dim + 8 * sub);
+    const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0 && m > 0.f) atomicMax(p.amax_bits + h, __float_as_uint(m));  // non-negative: bits order as values
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) warp_max[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = 0.f;
+#pragma unroll
+    for (int i = 0; i < kAmaxThreads / 32; ++i) b = fmaxf(b, warp_max[i]);
+    if (b > 0.f) atomicMax(p.amax_bits + h, __float_as_uint(b));
   }
 }
 
@@ -75,9 +93,12 @@ __global__ void __launch_bounds__(kQuantThreads) v_quant_kernel(const PrepassPar
   const uint32_t bits = p.amax_bits[h];
   const float amax = __uint_as_float(bits);
   const float inv = amax > 0.f ? kE4m3Max / amax : 1.f;
-  // phase 1: 128 positions x 16 chunks of 8 head dims; thread -> (position, chunk)
-  for (int it = threadIdx.x; it < 128 * 16; it += kQuantThreads) {
-    const int r = it >> 4, c = it & 15;
+  // phase 1: one padded key position per lane (warps 0-3 head dims 0..63,
+  // warps 4-7 head dims 64..127): each byte store of a warp writes 32
+  // consecutive bytes of one row of the tile (no bank conflicts)
+  {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = 32 * (warp & 3) + lane;
     const int64_t x = x0 + r;
     // the sequence whose padded range holds x (binary search on padded starts)
     int lo = 0, hi = p.batch - 1;
@@ -91,20 +112,30 @@ __global__ void __launch_bounds__(kQuantThreads) v_quant_kernel(const PrepassPar
     const int64_t ks = seq_key_start(p, lo);
     const int64_t len = p.cu_k != nullptr ? static_cast<int64_t>(p.cu_k[lo + 1]) - ks : p.max_seqlen_k;
     const int64_t i = x - padded_start(ks, lo);
-    uint16_t q[4] = {0, 0, 0, 0};
-    if (p.batch > 0 && i >= 0 && i < len) {
-      const uint4 v4 = *reinterpret_cast<const uint4*>(p.v + ((ks + i) * p.kv_heads + h) * p.head_dim + 8 * c);
-      const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
+    const bool in_seq = p.batch > 0 && i >= 0 && i < len;
+    const __nv_bfloat16* src = p.v + ((ks + i) * p.kv_heads + h) * p.head_dim;
+    uint4 rowv[8];  // this lane's 8 chunks of 8 head dims, all loads in flight at once
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      rowv[i] = in_seq ? *reinterpret_cast<const uint4*>(src + 8 * (8 * (warp >> 2) + i)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = 8 * (warp >> 2) + i;
+      uint16_t q[4] = {0, 0, 0, 0};
+      if (in_seq) {
+        const uint4 v4 = rowv[i];
+        const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+          q[k] = e4m3x2(f.x * inv, f.y * inv);
+        }
+      }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
-        q[k] = e4m3x2(f.x * inv, f.y * inv);
+        tile[8 * c + 2 * k][r] = static_cast<uint8_t>(q[k] & 0xffu);
+        tile[8 * c + 2 * k + 1][r] = static_cast<uint8_t>(q[k] >> 8);
       }
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      tile[8 * c + 2 * k][r] = static_cast<uint8_t>(q[k] & 0xffu);
-      tile[8 * c + 2 * k + 1][r] = static_cast<uint8_t>(q[k] >> 8);
     }
   }
   __syncthreads();
