@@ -371,7 +371,7 @@ extern "C" int fmha_bwd(const void* q, const void* k, const void* v, const void*
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
   }
   if (qblocks > 0 && total_q > 0) {
-    fmha::bwd::fmha_bwd_dq_kernel<<<dim3(heads, qblocks, batch), fmha::bwd::kThreads, fmha::bwd::DqSmem::kBytes,
+    fmha::bwd::fmha_bwd_dq_kernel<<<dim3(heads, qblocks, batch), fmha::bwd::kDqThreads, fmha::bwd::DqSmem::kBytes,
                                     st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
   }

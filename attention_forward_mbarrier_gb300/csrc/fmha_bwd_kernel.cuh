@@ -41,6 +41,9 @@ namespace bwd {
 constexpr int kThreads = 192;
 constexpr int kWarpProducer = 4;
 constexpr int kWarpMma = 5;
+// the dQ kernel has a second MMA-issuing warp for dP (224 threads)
+constexpr int kDqThreads = 224;
+constexpr int kWarpMmaDp = 6;
 constexpr uint32_t kTile = kBlockM * 128 * 2;  // a 128 x 128 bf16 tile: two swizzled 64-column halves
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -158,11 +161,13 @@ constexpr int kDqQFull = 0;     // Q and dO landed
 constexpr int kDqKFull = 1;     // [3] K_j of slot j % 3 landed
 constexpr int kDqVFull = 4;     // [2] V_j of slot j % 2 landed
 constexpr int kDqKFree = 6;     // [3] dQ(j) retired: K_j no longer read
-constexpr int kDqBlkReady = 9;  // [2] S(j) and dP(j) in TMEM, barrier j & 1; also tells the
-                                // producer that V_j (read only by dP(j)) is free
+constexpr int kDqBlkReady = 9;  // [2] S(j) and dP(j) in TMEM, barrier j & 1 (two arrivals: the S
+                                // issuer's and the dP issuer's commits); also tells the producer
+                                // that V_j (read only by dP(j)) is free
 constexpr int kDqDpFree = 11;   // dP(j) read into registers (4 warps)
 constexpr int kDqPReady = 12;   // [2] dS(j) stored, barrier j & 1 (4 warps)
-constexpr int kDqDone = 14;     // every MMA retired
+constexpr int kDqDone = 14;     // every MMA of the S / dQ issuer retired
+constexpr int kDqDpDone = 15;   // every MMA of the dP issuer retired
 // Pairs of alternating barriers where a waiter could otherwise find a barrier
 // two phases on: dP(j+1) lets the gradient warps finish block j+1 before the
 // MMA thread polls for dS(j), and dP(j+1) may retire before the producer polls
@@ -174,11 +179,13 @@ constexpr int kDqDone = 14;     // every MMA retired
 constexpr uint32_t kDqColDp = 256, kDqColDq = 384;
 __device__ __forceinline__ uint32_t dq_col_s(int j) { return 128u * static_cast<uint32_t>(j & 1); }
 
-// Schedule (one MMA-issuing thread): S(0), dP(0), S(1); then per block j:
-// dP(j+1) as soon as the gradient warps have dP(j) in registers, dQ(j) once
-// dS(j) is stored, S(j+2) into the S buffer dQ(j) just read.  The gradient
-// math of block j thus overlaps dP(j+1) and the S products of later blocks.
-__global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+// Schedule (two MMA-issuing threads; issue is paced by the tensor pipe, so a
+// thread blocked on its own queue cannot react to a hand-off): the S / dQ
+// issuer issues S(0), S(1), then per block j dQ(j) once dS(j) is stored and
+// S(j+2) into the S buffer dQ(j) just read; the dP issuer issues dP(j+1) as
+// soon as the gradient warps have dP(j) in registers.  The gradient math of
+// block j thus overlaps dP(j+1) and the S products of later blocks.
+__global__ void __launch_bounds__(kDqThreads, 1) fmha_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -237,8 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
       ptx::mbar_init(ctx.bar(kDqKFree + s), 1);
     }
     for (int s = 0; s < kDqVSlots; ++s) ptx::mbar_init(ctx.bar(kDqVFull + s), 1);
-    ptx::mbar_init(ctx.bar(kDqBlkReady), 1);
-    ptx::mbar_init(ctx.bar(kDqBlkReady + 1), 1);
+    ptx::mbar_init(ctx.bar(kDqBlkReady), 2);
+    ptx::mbar_init(ctx.bar(kDqBlkReady + 1), 2);
+    ptx::mbar_init(ctx.bar(kDqDpDone), 1);
     ptx::mbar_init(ctx.bar(kDqDpFree), 4);
     ptx::mbar_init(ctx.bar(kDqPReady), 4);
     ptx::mbar_init(ctx.bar(kDqPReady + 1), 4);
@@ -388,26 +396,23 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
       if (nb > 0) wait_drain(ctx, kDqQFull, 0);
     }
     __syncwarp();
-  } else {
-    // ================================ MMA issuer
+  } else if (warp == kWarpMma) {
+    // ================================ S / dQ issuer
     if (lane == 0 && nb > 0) {
       const uint64_t q_desc = desc_kmajor(base + DqSmem::kOffQ);
-      const uint64_t do_desc = desc_kmajor(base + DqSmem::kOffDo);
       const uint64_t k_kmaj = desc_kmajor(base + DqSmem::kOffK);
       const uint64_t k_mn = desc_mnmajor(base + DqSmem::kOffK);
-      const uint64_t v_kmaj = desc_kmajor(base + DqSmem::kOffV);
       constexpr uint64_t kStep = kTile >> 4;  // descriptor units of one tile
       auto wait_k = [&](int j) { return wait_bar(ctx, kDqKFull + j % kDqKSlots, (j / kDqKSlots) & 1, kRoleMma); };
-      auto wait_v = [&](int j) { return wait_bar(ctx, kDqVFull + j % kDqVSlots, (j / kDqVSlots) & 1, kRoleMma); };
-      auto issue_s = [&](int j) { issue_qk<128>(tmem + dq_col_s(j), q_desc, k_kmaj + (j % kDqKSlots) * kStep); };
-      auto issue_dp = [&](int j) { issue_qk<128>(tmem + kDqColDp, do_desc, v_kmaj + (j % kDqVSlots) * kStep); };
+      auto issue_s = [&](int j) {
+        issue_qk<128>(tmem + dq_col_s(j), q_desc, k_kmaj + (j % kDqKSlots) * kStep);
+        ptx::mma_commit(ctx.bar(kDqBlkReady + (j & 1)));  // S(j): one of block j's two arrivals
+      };
       bool issued_any = false;
-      bool ok = wait_bar(ctx, kDqQFull, 0, kRoleMma) && wait_k(0) && wait_v(0);
+      bool ok = wait_bar(ctx, kDqQFull, 0, kRoleMma) && wait_k(0);
       if (ok) {
         ptx::tc_fence_after();
         issue_s(0);
-        issue_dp(0);
-        ptx::mma_commit(ctx.bar(kDqBlkReady));  // block 0
         issued_any = true;
         if (nb > 1) {
           ok = wait_k(1);
@@ -418,16 +423,6 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
         }
       }
       for (int j = 0; j < nb && ok; ++j) {
-        if (j + 1 < nb) {
-          // dP(j) is in the gradient warps' registers: dP(j+1) into its columns
-          if (!wait_bar(ctx, kDqDpFree, j & 1, kRoleMma)) break;
-          if (j < 64) FMHA_BWD_TRACE(trow, 8 * j + 3);
-          if (!wait_v(j + 1)) break;
-          if (j < 64) FMHA_BWD_TRACE(trow, 8 * j + 6);
-          ptx::tc_fence_after();
-          issue_dp(j + 1);
-          ptx::mma_commit(ctx.bar(kDqBlkReady + ((j + 1) & 1)));  // block j+1: S(j+1) was issued earlier
-        }
         if (!wait_bar(ctx, kDqPReady + (j & 1), (j >> 1) & 1, kRoleMma)) break;
         if (j < 64) FMHA_BWD_TRACE(trow, 8 * j + 4);
         ptx::tc_fence_after();
@@ -444,6 +439,33 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dq_kernel(const __grid_c
       if (issued_any) {
         ptx::mma_commit(ctx.bar(kDqDone));
         wait_drain(ctx, kDqDone, 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMmaDp) {
+    // ================================ dP issuer
+    if (lane == 0 && nb > 0) {
+      const uint64_t do_desc = desc_kmajor(base + DqSmem::kOffDo);
+      const uint64_t v_kmaj = desc_kmajor(base + DqSmem::kOffV);
+      constexpr uint64_t kStep = kTile >> 4;
+      bool issued_any = false;
+      bool ok = wait_bar(ctx, kDqQFull, 0, kRoleMma);
+      for (int j = 0; j < nb && ok; ++j) {
+        if (j > 0) {
+          // dP(j-1) is in the gradient warps' registers: dP(j) into its columns
+          if (!wait_bar(ctx, kDqDpFree, (j - 1) & 1, kRoleMma)) break;
+          if (j - 1 < 64) FMHA_BWD_TRACE(trow, 8 * (j - 1) + 3);
+        }
+        if (!wait_bar(ctx, kDqVFull + j % kDqVSlots, (j / kDqVSlots) & 1, kRoleMma)) break;
+        if (j > 0 && j - 1 < 64) FMHA_BWD_TRACE(trow, 8 * (j - 1) + 6);
+        ptx::tc_fence_after();
+        issue_qk<128>(tmem + kDqColDp, do_desc, v_kmaj + (j % kDqVSlots) * kStep);  // dP(j) = dO V_j^T
+        ptx::mma_commit(ctx.bar(kDqBlkReady + (j & 1)));  // dP(j): block j's other arrival
+        issued_any = true;
+      }
+      if (issued_any) {
+        ptx::mma_commit(ctx.bar(kDqDpDone));
+        wait_drain(ctx, kDqDpDone, 0);
       }
     }
     __syncwarp();
