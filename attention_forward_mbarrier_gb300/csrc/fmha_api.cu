@@ -376,7 +376,7 @@ extern "C" int fmha_bwd(const void* q, const void* k, const void* v, const void*
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
   }
   if (kblocks > 0 && total_k > 0) {
-    fmha::bwd::fmha_bwd_dkdv_kernel<<<dim3(kv_heads, kblocks, batch), fmha::bwd::kThreads,
+    fmha::bwd::fmha_bwd_dkdv_kernel<<<dim3(kv_heads, kblocks, batch), fmha::bwd::kDkvThreads,
                                       fmha::bwd::DkvSmem::kBytes, st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
   }

@@ -28,8 +28,9 @@
 //                         overlaps the other half's products.
 // Every GEMM is a tcgen05.mma of one of the forward's two forms: both operands
 // K-major in shared memory, or A from TMEM with an MN-major B.  Warp roles
-// (192 threads): warps 0-3 the gradient math on one TMEM lane (row) each and
-// the epilogue; warp 4 the TMA producer; warp 5 the MMA issuer and TMEM owner.
+// (224 threads): warps 0-3 the gradient math on one TMEM lane (row) each and
+// the epilogue; warp 4 the TMA producer; warps 5 and 6 issue MMAs (two
+// streams, see each kernel), warp 5 owns TMEM.
 // Every mbarrier wait is bounded as in the forward kernel.
 #pragma once
 
@@ -38,7 +39,6 @@
 namespace fmha {
 namespace bwd {
 
-constexpr int kThreads = 192;
 constexpr int kWarpProducer = 4;
 constexpr int kWarpMma = 5;
 // the dQ kernel has a second MMA-issuing warp for dP (224 threads)
@@ -69,8 +69,9 @@ struct alignas(64) BwdParams {
 
 // Opt-in coarse trace (build with -DFMHA_TRACE): %clock64 stamps of the CTAs
 // of head (K/V head) 0, sequence 0, one row of kTraceSlots per query (key)
-// block: per block / item j < 64 at slot 8 j + event, set-up and exit at
-// 1000 + event.
+// block: per block / item j < 64 at slot 8 j + event, the dK/dV kernel's
+// issuing threads per item j < 60 at slot 512 + 8 j + event, set-up and exit
+// at 1000 + event.
 #ifdef FMHA_TRACE
 __device__ unsigned long long* g_trace_dq;
 __device__ unsigned long long* g_trace_dkdv;
@@ -496,7 +497,10 @@ constexpr int kKvStageFull = 1;   // [2] Q, dO and the row terms of stage s
 constexpr int kKvStageFree = 3;   // [2] the MMAs reading stage s retired
 constexpr int kKvHalfReady = 5;   // [2] S^T, dP^T of query half h in TMEM
 constexpr int kKvPReady = 7;      // [2] P^T, dS^T of query half h stored (4 warps)
-constexpr int kKvDone = 9;        // every MMA retired
+constexpr int kKvDone = 9;        // every MMA of the dV / dK issuer retired
+constexpr int kKvDvDone = 10;     // [2] dV, dK of query half h retired: its TMEM columns are free
+constexpr int kKvScoreDone = 12;  // every MMA of the score issuer retired
+constexpr int kDkvThreads = 224;  // two MMA-issuing warps: scores (warp 5), dV / dK (warp 6)
 // TMEM columns.  Each 128-query block is processed as two halves of 64
 // queries: S^T of half h at 64 h, dP^T at 128 + 64 h (P^T and dS^T as bf16
 // over their first 32 columns), dV at 256, dK at 384.
@@ -529,7 +533,7 @@ __device__ __forceinline__ void issue_half_pv(uint32_t tmem_d, uint32_t tmem_a, 
   for (int k = 1; k < 4; ++k) ptx::mma_ts_imm<true>(tmem_d, tmem_a + 8u * k, b_desc + ((2048u * k) >> 4), idesc);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kDkvThreads, 1) fmha_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -576,8 +580,10 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid
       ptx::mbar_init(ctx.bar(kKvStageFree + s), 1);
       ptx::mbar_init(ctx.bar(kKvHalfReady + s), 1);
       ptx::mbar_init(ctx.bar(kKvPReady + s), 4);
+      ptx::mbar_init(ctx.bar(kKvDvDone + s), 1);
     }
     ptx::mbar_init(ctx.bar(kKvDone), 1);
+    ptx::mbar_init(ctx.bar(kKvScoreDone), 1);
     *ctx.abort_flag = 0u;
     ptx::fence_mbar_init();
     if (n_items > 0) {
@@ -744,35 +750,56 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid
       if (n_items > 0) wait_drain(ctx, kKvKVFull, 0);
     }
     __syncwarp();
-  } else {
-    // ================================ MMA issuer
-    // Per item (query block), per half h of 64 queries: dV/dK of item it, half
-    // h, as soon as its P^T/dS^T are stored, then S^T/dP^T of item it + 1,
-    // half h into the columns those products just read.  The gradient math of
-    // one half overlaps the tensor work of the other.
+  } else if (warp == kWarpMma) {
+    // ================================ score issuer
+    // Per item (query block), per half h of 64 queries: S^T and dP^T into the
+    // half's columns once the dV / dK issuer's products of the previous item
+    // have read them.  Two issuing threads because issue is paced by the
+    // tensor pipe: one thread blocked on its own queue would see the other
+    // stream's hand-offs late.
     if (lane == 0 && n_items > 0) {
       const uint64_t k_desc = desc_kmajor(base + DkvSmem::kOffK);
       const uint64_t v_desc = desc_kmajor(base + DkvSmem::kOffV);
-      constexpr uint64_t kStep = kTile >> 4;
       constexpr uint64_t kHalfRows = kQHalfBytes >> 4;  // rows 64.. of a tile, in descriptor units
-      auto q_tile = [&](int it) { return base + DkvSmem::kOffRing + 2u * (it & 1) * kTile; };
-      auto issue_scores = [&](int it, int hf) {
-        const uint64_t q_kmaj = desc_kmajor(q_tile(it)) + hf * kHalfRows;
-        const uint64_t do_kmaj = desc_kmajor(q_tile(it) + kTile) + hf * kHalfRows;
-        issue_half_qk(tmem + 64u * hf, k_desc, q_kmaj);             // S^T_h = K Q_h^T
-        issue_half_qk(tmem + kKvColDp + 64u * hf, v_desc, do_kmaj);  // dP^T_h = V dO_h^T
-        ptx::mma_commit(ctx.bar(kKvHalfReady + hf));
-      };
       bool issued_any = false;
-      bool ok = wait_bar(ctx, kKvKVFull, 0, kRoleMma) && wait_bar(ctx, kKvStageFull, 0, kRoleMma);
-      if (ok) {
-        ptx::tc_fence_after();
-        issue_scores(0, 0);
-        issue_scores(0, 1);
-        issued_any = true;
-      }
+      bool ok = wait_bar(ctx, kKvKVFull, 0, kRoleMma);
       for (int it = 0; it < n_items && ok; ++it) {
-        const int s = it & 1;
+        const uint32_t q_tile = base + DkvSmem::kOffRing + 2u * (it & 1) * kTile;
+        if (!wait_bar(ctx, kKvStageFull + (it & 1), (it >> 1) & 1, kRoleMma)) break;
+        if (it < 60) FMHA_BWD_TRACE(trow, 512 + 8 * it + 0);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          if (it > 0 && !wait_bar(ctx, kKvDvDone + hf, (it - 1) & 1, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          if (it < 60) FMHA_BWD_TRACE(trow, 512 + 8 * it + 1 + hf);
+          ptx::tc_fence_after();
+          const uint64_t q_kmaj = desc_kmajor(q_tile) + hf * kHalfRows;
+          const uint64_t do_kmaj = desc_kmajor(q_tile + kTile) + hf * kHalfRows;
+          issue_half_qk(tmem + 64u * hf, k_desc, q_kmaj);             // S^T_h = K Q_h^T
+          issue_half_qk(tmem + kKvColDp + 64u * hf, v_desc, do_kmaj);  // dP^T_h = V dO_h^T
+          ptx::mma_commit(ctx.bar(kKvHalfReady + hf));
+          if (hf == 1 && it < 60) FMHA_BWD_TRACE(trow, 512 + 8 * it + 3);
+          issued_any = true;
+        }
+      }
+      if (issued_any) {
+        ptx::mma_commit(ctx.bar(kKvScoreDone));
+        wait_drain(ctx, kKvScoreDone, 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma + 1) {
+    // ================================ dV / dK issuer
+    if (lane == 0 && n_items > 0) {
+      constexpr uint64_t kHalfRows = kQHalfBytes >> 4;
+      bool issued_any = false;
+      bool ok = true;
+      for (int it = 0; it < n_items && ok; ++it) {
+        const uint32_t q_tile = base + DkvSmem::kOffRing + 2u * (it & 1) * kTile;
+        // the item's Q and dO tiles (complete by now; observed by this thread too)
+        if (!wait_bar(ctx, kKvStageFull + (it & 1), (it >> 1) & 1, kRoleMma)) break;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           if (!wait_bar(ctx, kKvPReady + hf, it & 1, kRoleMma)) {
@@ -782,21 +809,14 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_bwd_dkdv_kernel(const __grid
           if (it < 64) FMHA_BWD_TRACE(trow, 8 * it + 5 + hf);
           ptx::tc_fence_after();
           const bool acc = it > 0 || hf > 0;
-          const uint64_t q_mn = desc_mnmajor(q_tile(it)) + hf * kHalfRows;
-          const uint64_t do_mn = desc_mnmajor(q_tile(it) + kTile) + hf * kHalfRows;
+          const uint64_t q_mn = desc_mnmajor(q_tile) + hf * kHalfRows;
+          const uint64_t do_mn = desc_mnmajor(q_tile + kTile) + hf * kHalfRows;
           issue_half_pv(tmem + kKvColDv, tmem + 64u * hf, do_mn, acc);             // dV += P^T_h dO_h
           issue_half_pv(tmem + kKvColDk, tmem + kKvColDp + 64u * hf, q_mn, acc);   // dK += dS^T_h Q_h
-          if (hf == 1) ptx::mma_commit(ctx.bar(kKvStageFree + s));
-          if (it + 1 < n_items) {
-            if (hf == 0) {
-              if (!wait_bar(ctx, kKvStageFull + ((it + 1) & 1), ((it + 1) >> 1) & 1, kRoleMma)) {
-                ok = false;
-                break;
-              }
-              ptx::tc_fence_after();
-            }
-            issue_scores(it + 1, hf);
-          }
+          ptx::mma_commit(ctx.bar(kKvDvDone + hf));
+          if (hf == 1) ptx::mma_commit(ctx.bar(kKvStageFree + (it & 1)));  // the item's Q, dO read by both issuers
+          if (it < 60) FMHA_BWD_TRACE(trow, 512 + 8 * it + 4 + hf);
+          issued_any = true;
         }
       }
       if (issued_any) {
