@@ -19,6 +19,7 @@
 
 #include "fmha.h"
 #include "fmha_fwd_kernel.cuh"
+#include "fmha_fwd_persistent.cuh"
 #include "fmha_bwd_kernel.cuh"
 #include "fmha_fp8_prepass.cuh"
 
@@ -84,6 +85,72 @@ int launch(const fmha::FwdParams& p, dim3 grid, fmha_stream_t stream) {
   if (configure_kernel<HD, kGrouped, kFp8>() != 0) return FMHA_ERR_CUDA;
   fmha::fmha_fwd_kernel<HD, kGrouped, kFp8><<<grid, fmha::kThreads, fmha::Dims<HD>::kSmemBytes,
                                               reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
+}
+
+// The persistent kernel runs when the plain grid would take more than
+// FMHA_PERSISTENT_WAVES waves of CTAs (one CTA per SM), i.e. when many units
+// would each pay their own set-up and epilogue.  Test builds lower the
+// threshold and cap the grid (FMHA_PERSISTENT_MAX_CTAS) so that small problems
+// run many units per CTA.
+#ifndef FMHA_PERSISTENT_WAVES
+#define FMHA_PERSISTENT_WAVES 1
+#endif
+#ifndef FMHA_PERSISTENT_MAX_CTAS
+#define FMHA_PERSISTENT_MAX_CTAS 0
+#endif
+
+template <int HD>
+int configure_persistent() {
+  static int rc = -1;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (rc != 0) {
+    rc = cudaFuncSetAttribute(fmha::fmha_fwd_persistent_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(fmha::pers::Smem<HD>::kBytes)) == cudaSuccess
+             ? 0
+             : 1;
+  }
+  return rc;
+}
+
+// SM count of the current device (cached per device).
+int sm_count() {
+  static int counts[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+// A counter slot of the persistent kernel for this launch: slots are handed
+// out round-robin, so launches in flight at the same time use different ones.
+unsigned int* work_slot() {
+  static void* base[64] = {nullptr};
+  static std::mutex mu;
+  static unsigned int next = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (base[dev] == nullptr && cudaGetSymbolAddress(&base[dev], fmha::g_work) != cudaSuccess) {
+    base[dev] = nullptr;
+    return nullptr;
+  }
+  const unsigned int s = next++ % fmha::kWorkSlots;
+  return static_cast<unsigned int*>(base[dev]) + 2 * s;
+}
+
+template <int HD>
+int launch_persistent(fmha::FwdParams& p, int ctas, fmha_stream_t stream) {
+  if (configure_persistent<HD>() != 0) return FMHA_ERR_CUDA;
+  p.work = work_slot();
+  if (p.work == nullptr) return FMHA_ERR_CUDA;
+  fmha::fmha_fwd_persistent_kernel<HD><<<ctas, fmha::kThreads, fmha::pers::Smem<HD>::kBytes,
+                                         reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
 }
 
@@ -171,6 +238,15 @@ extern "C" int fmha_fwd_gqa(const void* q, const void* k, const void* v, void* o
   if (grouped) {
     const dim3 grid(static_cast<unsigned>(heads * pairs), static_cast<unsigned>(batch), 1u);
     return head_dim == 64 ? launch<64, true>(p, grid, stream) : launch<128, true>(p, grid, stream);
+  }
+  const int64_t units = static_cast<int64_t>(heads) * pairs * batch;
+  const int sms = sm_count();
+  if (head_dim != 256 && sms > 0 && units > static_cast<int64_t>(FMHA_PERSISTENT_WAVES) * sms && units <= INT32_MAX / 2) {
+    int ctas = sms;
+    if (FMHA_PERSISTENT_MAX_CTAS > 0) ctas = std::min(ctas, FMHA_PERSISTENT_MAX_CTAS);
+    ctas = static_cast<int>(std::min<int64_t>(ctas, units));
+    p.units = static_cast<int>(units);
+    return head_dim == 64 ? launch_persistent<64>(p, ctas, stream) : launch_persistent<128>(p, ctas, stream);
   }
   const dim3 grid(static_cast<unsigned>(heads), static_cast<unsigned>(pairs), static_cast<unsigned>(batch));
   if (head_dim == 64) return launch<64, false>(p, grid, stream);
@@ -478,6 +554,20 @@ extern "C" int fmha_debug_set_bwd_trace(void* dq_buffer, void* dkdv_buffer) {
   unsigned long long* b = static_cast<unsigned long long*>(dkdv_buffer);
   if (cudaMemcpyToSymbol(fmha::bwd::g_trace_dq, &a, sizeof(a)) != cudaSuccess) return FMHA_ERR_CUDA;
   return cudaMemcpyToSymbol(fmha::bwd::g_trace_dkdv, &b, sizeof(b)) == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
+}
+
+// Trace builds only: persistent-kernel stamps, (grid size) x 64 units x 16
+// uint64 slots, or nullptr.
+extern "C" int fmha_debug_set_pers_trace(void* device_buffer) {
+  unsigned long long* p = static_cast<unsigned long long*>(device_buffer);
+  return cudaMemcpyToSymbol(fmha::pers::g_trace_pers, &p, sizeof(p)) == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
+}
+
+// Trace builds only: persistent-kernel observer stamps, (grid size) x 2 x 1024
+// uint64 slots, or nullptr.
+extern "C" int fmha_debug_set_pers_obs_trace(void* device_buffer) {
+  unsigned long long* p = static_cast<unsigned long long*>(device_buffer);
+  return cudaMemcpyToSymbol(fmha::pers::g_trace_obs, &p, sizeof(p)) == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
 }
 
 // Trace builds only: per-CTA table of 4 uint64 per CTA (grid size x 4), or nullptr.

@@ -162,6 +162,9 @@ struct alignas(64) FwdParams {
   // FP8 PV variant only
   const uint32_t* v_amax_bits;  // max |V| per K/V head (float bits)
   CUtensorMap tmap_vt;          // e4m3 V^T [kv_heads * 128, kpad] bytes, box 128 x 128, 128B swizzle
+  // persistent variant only
+  unsigned int* work;  // the launch's counter slot: {units fetched beyond the grid size, CTAs finished}
+  int units;           // heads * query blocks * sequences, in the plain grid's order
 };
 
 __device__ int g_status;  // 0 = ok, else 1 + (role * 256 + barrier id) of the first expired wait

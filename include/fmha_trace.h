@@ -37,6 +37,23 @@ int fmha_debug_set_cta_trace(void *device_buffer);
  */
 int fmha_debug_set_bwd_trace(void *dq_buffer, void *dkdv_buffer);
 
+/*
+ * fmha_debug_set_pers_trace -- caller-owned device memory of (grid size) x 64
+ * x 16 uint64, or NULL: the persistent forward kernel's stamps, per CTA and per
+ * unit it ran (the first 63), at the slots that fmha_fwd_persistent.cuh
+ * lists (unit index, %clock64 at the MMA warp's and the softmax warps'
+ * hand-offs, key blocks).  Returns FMHA_OK or FMHA_ERR_CUDA.
+ */
+int fmha_debug_set_pers_trace(void *device_buffer);
+
+/*
+ * fmha_debug_set_pers_obs_trace -- caller-owned device memory of (grid size)
+ * x 2 x 1024 uint64, or NULL: in the persistent forward kernel's trace build,
+ * two otherwise idle warps stamp (%clock64) when each step commit completes
+ * and when each ring load lands, in order (the first 1024 of each).
+ */
+int fmha_debug_set_pers_obs_trace(void *device_buffer);
+
 #ifdef __cplusplus
 }
 #endif
