@@ -10,7 +10,13 @@ Tuning", section "2. Trace the real pipeline, coarsely": stamps only at
 hand-offs, numbers in SM cycles.
 
   python -m attention_forward_mbarrier_gb300.trace [--workload NAME] [--row R]
-         [--flags "-DNAME=VALUE ..."] [--raw stamps.npy]
+         [--flags=-DNAME=VALUE ...] [--raw stamps.npy] [--persistent]
+
+The plain kernel is traced with the persistent variant switched off
+(-DFMHA_PERSISTENT_WAVES=1000000), so every workload runs it.  --persistent
+traces the persistent variant instead (fmha_fwd_persistent.cuh): per unit
+each CTA ran, the hand-offs around the boundary between consecutive units,
+and (from two observer warps) when step commits complete and ring loads land.
 """
 from __future__ import annotations
 
@@ -236,6 +242,99 @@ def summarize(row: np.ndarray) -> dict:
     return out
 
 
+PERS_UNITS, PERS_EVENTS = 64, 16  # the persistent kernel's trace slots per CTA
+
+
+def run_persistent(w: wl.Workload, repeats: int = 3, flags=()):
+    """Stamps of the persistent kernel's last launch: per CTA [units, events]
+    and the observers' [2, 1024] rows (step commits completed, loads landed)."""
+    L = load_trace_lib(flags)
+    L.fmha_debug_set_pers_trace.restype = ctypes.c_int
+    L.fmha_debug_set_pers_trace.argtypes = [ctypes.c_void_p]
+    L.fmha_debug_set_pers_obs_trace.restype = ctypes.c_int
+    L.fmha_debug_set_pers_obs_trace.argtypes = [ctypes.c_void_p]
+    dev = torch.device("cuda:0")
+    inp = wl.make_inputs(w, seed=0)
+    q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
+    cq = None if inp.cu_seqlens_q is None else inp.cu_seqlens_q.to(dev)
+    ck = None if inp.cu_seqlens_k is None else inp.cu_seqlens_k.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.heads, w.total_q), dtype=torch.float32, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    buf = torch.zeros((sms, PERS_UNITS, PERS_EVENTS), dtype=torch.int64, device=dev)
+    obs = torch.zeros((sms, 2, 1024), dtype=torch.int64, device=dev)
+    for _ in range(repeats):
+        buf.zero_()
+        obs.zero_()
+        L.fmha_debug_set_pers_trace(ctypes.c_void_p(buf.data_ptr()))
+        L.fmha_debug_set_pers_obs_trace(ctypes.c_void_p(obs.data_ptr()))
+        rc = L.fmha_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                        None if cq is None else cq.data_ptr(), None if ck is None else ck.data_ptr(),
+                        w.batch, w.total_q, w.total_k, w.max_seqlen_q, w.max_seqlen_k, w.heads, w.head_dim,
+                        w.softmax_scale, int(w.causal), None)
+        if rc != 0:
+            raise RuntimeError(f"fmha_fwd returned {rc}")
+        torch.cuda.synchronize()
+    L.fmha_debug_set_pers_trace(None)
+    L.fmha_debug_set_pers_obs_trace(None)
+    return buf.cpu().numpy(), obs.cpu().numpy()
+
+
+def summarize_persistent(a: np.ndarray, ob: np.ndarray) -> dict:
+    """Per-unit cycles by key blocks, and the boundary between consecutive
+    units of a CTA relative to the previous unit's last step commit (issue)."""
+    med = lambda v: float(np.median(v)) if len(v) else None  # noqa: E731
+    cta = a[:, PERS_UNITS - 1, :]
+    live = cta[cta[:, 0] != 0]
+    g0 = live[:, 0].min()
+    res = {"ctas": int(len(live)),
+           "cta_end_ns_min_med_max": [int(x) for x in np.percentile(live[:, 1] - g0, [0, 50, 100])],
+           "sm_clock_mhz_median": med((live[:, 3] - live[:, 2]) / (live[:, 1] - live[:, 0]) * 1e3)}
+    dur, gaps, per_cta = {}, [], []
+    bd = {k: [] for k in ("published", "q0_issued", "k0_issued", "q1_issued", "unit_taken", "k0_seen", "q0_seen",
+                          "q1_seen", "qk1_issued", "first_commit")}
+    ev = {"published": 8, "q0_issued": 9, "k0_issued": 10, "q1_issued": 11, "unit_taken": 1, "k0_seen": 12,
+          "q0_seen": 13, "q1_seen": 14, "qk1_issued": 15, "first_commit": 2}
+    bo = {k: [] for k in ("prev_commit_n-1_done", "prev_last_commit_done", "first_commit_done", "k0_landed",
+                          "v0_landed")}
+    for c in range(a.shape[0]):
+        rows = [r for r in a[c][:PERS_UNITS - 1] if r[1] != 0]
+        per_cta.append(len(rows))
+        cn = ld = 0
+        for i, r in enumerate(rows):
+            n = int(r[7])
+            if r[2] and r[3]:
+                dur.setdefault(n, []).append(int(r[3] - r[2]))
+            if i + 1 < len(rows) and r[3] and n > 0 and int(rows[i + 1][7]) > 0:
+                T, nxt = int(r[3]), rows[i + 1]
+                if nxt[2]:
+                    gaps.append(int(nxt[2]) - T)
+                for k_, e in ev.items():
+                    if nxt[e]:
+                        bd[k_].append(int(nxt[e]) - T)
+                st, lo = ob[c, 0], ob[c, 1]
+                if cn + n < 1024 and st[cn + n]:
+                    bo["prev_last_commit_done"].append(int(st[cn + n]) - T)
+                if cn + n - 1 < 1024 and st[cn + n - 1]:
+                    bo["prev_commit_n-1_done"].append(int(st[cn + n - 1]) - T)
+                if cn + n + 1 < 1024 and st[cn + n + 1]:
+                    bo["first_commit_done"].append(int(st[cn + n + 1]) - T)
+                g = ld + 2 * n
+                if g + 1 < 1024 and lo[g]:
+                    bo["k0_landed"].append(int(lo[g]) - T)
+                if g + 1 < 1024 and lo[g + 1]:
+                    bo["v0_landed"].append(int(lo[g + 1]) - T)
+            cn += n + 1 if n > 0 else 0
+            ld += 2 * n
+    res["units_per_cta_min_med_max"] = [min(per_cta), med(per_cta), max(per_cta)]
+    res["unit_cycles_by_key_blocks"] = {int(k_): {"units": len(v_), "cycles": med(v_), "per_block": round(med(v_) / k_, 1)}
+                                        for k_, v_ in sorted(dur.items()) if k_ > 0}
+    res["boundary_gap_cycles"] = med(gaps)
+    res["boundary_rel_prev_last_commit"] = {k_: med(v_) for k_, v_ in bd.items()}
+    res["observers_rel_prev_last_commit"] = {k_: med(v_) for k_, v_ in bo.items()}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default=wl.C2.name, choices=sorted(wl.CONFIGS))
@@ -243,9 +342,14 @@ def main():
     ap.add_argument("--raw", default=None, help="save the raw stamps (.npy)")
     ap.add_argument("--flags", default="", help="extra -D flags for the trace build (tuning variants)")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush before each launch")
+    ap.add_argument("--persistent", action="store_true", help="trace the persistent variant")
     args = ap.parse_args()
     w = wl.CONFIGS[args.workload]
-    stamps, ctas = run(w, flags=args.flags.split(), flush_l2=not args.no_flush)
+    if args.persistent:
+        a, ob = run_persistent(w, flags=args.flags.split())
+        print(json.dumps({"workload": w.name, "flags": args.flags, "persistent": summarize_persistent(a, ob)}, indent=1))
+        return
+    stamps, ctas = run(w, flags=["-DFMHA_PERSISTENT_WAVES=1000000", *args.flags.split()], flush_l2=not args.no_flush)
     if args.raw:
         np.save(args.raw, stamps)
         np.save(args.raw.replace(".npy", "") + "_ctas.npy", ctas)
