@@ -113,6 +113,14 @@ static_assert(kPSplit >= 1 && kPSplit <= 4, "P split in quarters of the key bloc
 // before it, or an MMA reads P columns not yet written.
 constexpr int kPvStepsBeforeFull = 2 * kPSplit;
 static_assert(kPvStepsBeforeFull * 16 <= kPSplit * 32, "P split: consumer ahead of producer");
+// The same knob for the FP8 PV variant (its PV K-steps are 32 keys, one per
+// quarter), tuned separately: the pages report a 3/4 split best for an FP8 PV
+// on B300.
+#ifndef FMHA_P_SPLIT_FP8
+#define FMHA_P_SPLIT_FP8 4
+#endif
+constexpr int kPSplitFp8 = FMHA_P_SPLIT_FP8;
+static_assert(kPSplitFp8 >= 1 && kPSplitFp8 <= 4, "FP8 P split in quarters of the key block");
 
 
 // Warpgroup of each role.  Warp w reaches TMEM lanes 32 (w % 4) .. + 31, so
@@ -394,7 +402,7 @@ __device__ __forceinline__ float exp_pass(const float (&s)[128], float c, float 
 // (the O rescale, which must precede the first PV), the stores so far are made
 // visible (wait::st, fence) and `signal` is called (split hand-off).  Running
 // the rescale there rather than before the pass keeps fewer scores live.
-template <typename Before, typename Signal>
+template <int kSplit, typename Before, typename Signal>
 __device__ __forceinline__ float exp_pass_split(const float (&s)[128], float c, float m_ref, uint32_t t_s,
                                                 Before&& before, Signal&& signal) {
   const float neg_mc = isinf(m_ref) ? 0.f : -m_ref * c;
@@ -414,7 +422,7 @@ __device__ __forceinline__ float exp_pass_split(const float (&s)[128], float c, 
       pk[i] = ptx::pack_bf16x2(p0, p1);
     }
     ptx::tmem_st16(t_s + 16u * q, pk);
-    if (q == kPSplit - 1 && q < 3) {
+    if (q == kSplit - 1 && q < 3) {
       before();
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -481,6 +489,43 @@ __device__ __forceinline__ float exp_pass_fp8(const float (&s)[128], float c, fl
   return a.x + a.y;
 }
 
+// The FP8 exp pass in four 32-key chunks (8 TMEM columns each), with the
+// split hand-off of exp_pass_split after chunk kSplit - 1.
+template <int kSplit, typename Before, typename Signal>
+__device__ __forceinline__ float exp_pass_fp8_split(const float (&s)[128], float c, float m_ref, uint32_t t_s,
+                                                    Before&& before, Signal&& signal) {
+  const float neg_mc = isinf(m_ref) ? 0.f : -m_ref * c;
+  const float2 c2 = make_float2(c, c);
+  const float2 nm2 = make_float2(neg_mc, neg_mc);
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int k = q * 32 + 4 * i;
+      const float2 x0 = __ffma2_rn(make_float2(s[k], s[k + 1]), c2, nm2);
+      const float2 x1 = __ffma2_rn(make_float2(s[k + 2], s[k + 3]), c2, nm2);
+      const float p0 = ptx::ex2_approx(x0.x), p1 = ptx::ex2_approx(x0.y);
+      const float p2 = ptx::ex2_approx(x1.x), p3 = ptx::ex2_approx(x1.y);
+      acc[(2 * i) & 3] = __fadd2_rn(acc[(2 * i) & 3], make_float2(p0, p1));
+      acc[(2 * i + 1) & 3] = __fadd2_rn(acc[(2 * i + 1) & 3], make_float2(p2, p3));
+      pk[i] = pack_e4m3x2(p0, p1) | (pack_e4m3x2(p2, p3) << 16);
+    }
+    ptx::tmem_st8(t_s + 8u * q, pk);
+    if (q == kSplit - 1 && q < 3) {
+      before();
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      signal();
+    }
+  }
+  const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+  const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+  const float2 a = __fadd2_rn(a01, a23);
+  return a.x + a.y;
+}
+
 // O (+)= P V with e4m3 operands: M=128 queries, N=128 head dims, K=128 keys in
 // 4 steps of 32.  P from TMEM (8 columns of four keys per step); V^T K-major
 // in shared memory (128 head-dim rows of 128 key bytes, 128-byte swizzle):
@@ -495,6 +540,20 @@ __device__ __forceinline__ void issue_pv_fp8(uint32_t tmem_d, uint32_t tmem_p, u
   for (int k = 1; k < kBlockN / 32; ++k) ptx::mma_ts_f8_imm<true>(tmem_d, tmem_p + 8u * k, vt_desc + ((32u * k) >> 4), idesc);
 }
 
+// The FP8 PV over the K-steps [k0, k1) (32 keys each).
+__device__ __forceinline__ void issue_pv_fp8_steps(uint32_t tmem_d, uint32_t tmem_p, uint64_t vt_desc, bool accumulate,
+                                                   int k0, int k1) {
+  constexpr uint32_t idesc = ptx::idesc_e4m3_f32(kBlockM, 128);
+#pragma unroll
+  for (int k = 0; k < kBlockN / 32; ++k) {
+    if (k < k0 || k >= k1) continue;
+    if (k == 0 && !accumulate)
+      ptx::mma_ts_f8_imm<false>(tmem_d, tmem_p, vt_desc, idesc);
+    else
+      ptx::mma_ts_f8_imm<true>(tmem_d, tmem_p + 8u * k, vt_desc + ((32u * k) >> 4), idesc);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // kGrouped: the head-grouped grid order (see decode_grouped); else the grid
 // is (heads, query blocks, sequences).
@@ -503,7 +562,11 @@ __device__ __forceinline__ void issue_pv_fp8(uint32_t tmem_d, uint32_t tmem_p, u
 // epilogue's 1 / l.
 template <int HD, bool kGrouped, bool kFp8 = false>
 __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_constant__ FwdParams p) {
-  static_assert(!kFp8 || (HD == 128 && kPSplit == 4), "FP8 PV: head_dim 128, one P hand-off");
+  static_assert(!kFp8 || HD == 128, "FP8 PV: head_dim 128");
+  // the P hand-off split of this variant, and the PV K-steps issued after its first signal
+  constexpr int kSplit = kFp8 ? kPSplitFp8 : kPSplit;
+  constexpr int kStepsBeforeFull = kFp8 ? kSplit : kPvStepsBeforeFull;
+  static_assert(kStepsBeforeFull * (kFp8 ? 32 : 16) <= kSplit * 32, "P split: consumer ahead of producer");
   using D = Dims<HD>;
   constexpr int kHeadDim = HD;
   constexpr int kStages = D::kStages;
@@ -731,14 +794,17 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         }
       };
       float row_sum;
-      if constexpr (kFp8) {
+      auto signal_part = [&]() {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVPart + t));
+      };
+      if constexpr (kFp8 && kSplit < 4) {
+        row_sum = exp_pass_fp8_split<kSplit>(s, c, m_ref, t_s, rescale_o, signal_part);
+      } else if constexpr (kFp8) {
         row_sum = exp_pass_fp8(s, c, m_ref, t_s);
         rescale_o();
-      } else if constexpr (kPSplit < 4) {
-        row_sum = exp_pass_split(s, c, m_ref, t_s, rescale_o, [&]() {
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVPart + t));
-        });
+      } else if constexpr (kSplit < 4) {
+        row_sum = exp_pass_split<kSplit>(s, c, m_ref, t_s, rescale_o, signal_part);
       } else {
         row_sum = exp_pass(s, c, m_ref, t_s);
         rescale_o();
@@ -918,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
 #pragma unroll
             for (int t = 0; t < kTiles; ++t) {
               if (!ok || j >= n_blk(t)) continue;
-              if constexpr (kPSplit < 4) {
+              if constexpr (kSplit < 4) {
                 // split hand-off: the K-steps of the first P chunks after the
                 // first signal, the rest after the full one
                 if (!wait_bar(ctx, kBarPVPart + t, j & 1, kRoleMma)) {
@@ -926,8 +992,12 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
                   break;
                 }
                 ptx::tc_fence_after();
-                issue_pv_steps<HD>(tmem + col_o(t), tmem + col_s(t), kv_desc_mn + kSlotDescStep * vslot, j > 0, 0,
-                                   kPvStepsBeforeFull);
+                if constexpr (kFp8)
+                  issue_pv_fp8_steps(tmem + col_o(t), tmem + col_s(t), kv_desc + kSlotDescStep * vslot, j > 0, 0,
+                                     kStepsBeforeFull);
+                else
+                  issue_pv_steps<HD>(tmem + col_o(t), tmem + col_s(t), kv_desc_mn + kSlotDescStep * vslot, j > 0, 0,
+                                     kStepsBeforeFull);
               }
               if (!wait_bar(ctx, kBarPVReady + t, j & 1, kRoleMma)) {
                 ok = false;
@@ -935,9 +1005,12 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
               }
               if (tr) FMHA_TRACE_AT(kTrMma + j * 8 + 1 + 2 * t);
               ptx::tc_fence_after();
-              if constexpr (kPSplit < 4)
+              if constexpr (kFp8 && kSplit < 4)
+                issue_pv_fp8_steps(tmem + col_o(t), tmem + col_s(t), kv_desc + kSlotDescStep * vslot, j > 0,
+                                   kStepsBeforeFull, kBlockN / 32);
+              else if constexpr (kSplit < 4)
                 issue_pv_steps<HD>(tmem + col_o(t), tmem + col_s(t), kv_desc_mn + kSlotDescStep * vslot, j > 0,
-                                   kPvStepsBeforeFull, kBlockN / 16);
+                                   kStepsBeforeFull, kBlockN / 16);
               else if constexpr (kFp8)
                 issue_pv_fp8(tmem + col_o(t), tmem + col_s(t), kv_desc + kSlotDescStep * vslot, j > 0);
               else

@@ -343,6 +343,13 @@ __device__ __forceinline__ void tmem_ld32x2_wait(uint32_t ta, float (&a)[32], ui
 #undef FMHA_R32
 }
 
+// Store 8 consecutive 32-bit columns of this thread's TMEM lane (asynchronous).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // Store 16 consecutive 32-bit columns of this thread's TMEM lane (asynchronous).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
