@@ -73,7 +73,7 @@ int configure_kernel() {
   // per-process attribute; re-applied cheaply if a previous attempt failed
   if (rc != 0) {
     rc = cudaFuncSetAttribute(fmha::fmha_fwd_kernel<HD, kGrouped, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(fmha::Dims<HD>::kSmemBytes)) == cudaSuccess
+                              static_cast<int>(fmha::Dims<HD>::kSmemBytes + fmha::kTraceSmemBytes)) == cudaSuccess
              ? 0
              : 1;
   }
@@ -83,7 +83,7 @@ int configure_kernel() {
 template <int HD, bool kGrouped, bool kFp8 = false>
 int launch(const fmha::FwdParams& p, dim3 grid, fmha_stream_t stream) {
   if (configure_kernel<HD, kGrouped, kFp8>() != 0) return FMHA_ERR_CUDA;
-  fmha::fmha_fwd_kernel<HD, kGrouped, kFp8><<<grid, fmha::kThreads, fmha::Dims<HD>::kSmemBytes,
+  fmha::fmha_fwd_kernel<HD, kGrouped, kFp8><<<grid, fmha::kThreads, fmha::Dims<HD>::kSmemBytes + fmha::kTraceSmemBytes,
                                               reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
 }

@@ -196,11 +196,16 @@ __device__ unsigned long long* g_trace;
 // per-CTA table (every CTA, linear block id): %globaltimer at entry, after the
 // set-up sync and at exit, and the SM id
 __device__ unsigned long long* g_trace_ctas;
-#define FMHA_TRACE_AT(slot)                                                                 \
-  do {                                                                                      \
-    if (trace_row != nullptr) trace_row[(slot)] = static_cast<unsigned long long>(clock64()); \
+// The stamps go to shared memory (a global store would delay the thread's
+// next mbarrier arrive, which waits for its earlier stores, and so lengthen
+// the hand-offs being measured) and are copied to the row at exit.
+constexpr uint32_t kTraceSmemBytes = kTraceSlots * 8;
+#define FMHA_TRACE_AT(slot)                                                                  \
+  do {                                                                                       \
+    if (trace_row != nullptr) trace_smem[(slot)] = static_cast<unsigned long long>(clock64()); \
   } while (0)
 #else
+constexpr uint32_t kTraceSmemBytes = 0;
 #define FMHA_TRACE_AT(slot) \
   do {                      \
   } while (0)
@@ -616,7 +621,11 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
 #ifdef FMHA_TRACE
   unsigned long long* trace_row =
       (g_trace != nullptr && h == 0 && b == 0) ? g_trace + static_cast<size_t>(launch_pair) * kTraceSlots : nullptr;
-  if (threadIdx.x == 0 && trace_row != nullptr) trace_row[2] = t_entry;
+  // stamps in shared memory past the misc words (the trace build allocates kTraceSmemBytes more)
+  volatile unsigned long long* trace_smem = reinterpret_cast<volatile unsigned long long*>(smem + kOffMisc + 256);
+  if (trace_row != nullptr)
+    for (int i = threadIdx.x; i < kTraceSlots; i += blockDim.x) trace_smem[i] = 0ull;
+  if (threadIdx.x == 0 && trace_row != nullptr) trace_smem[2] = t_entry;
 #endif
   int q0, lq, k0, lk;
   if (p.cu_q != nullptr) {
@@ -1084,6 +1093,11 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     if (lane == 0 && g_trace_ctas != nullptr) g_trace_ctas[cta_lin * 4 + 2] = ptx::globaltimer_ns();
 #endif
   }
+#ifdef FMHA_TRACE
+  __syncthreads();
+  if (trace_row != nullptr)
+    for (int i = threadIdx.x; i < kTraceSlots; i += blockDim.x) trace_row[i] = trace_smem[i];
+#endif
 }
 
 }  // namespace fmha
