@@ -17,6 +17,9 @@ The plain kernel is traced with the persistent variant switched off
 traces the persistent variant instead (fmha_fwd_persistent.cuh): per unit
 each CTA ran, the hand-offs around the boundary between consecutive units,
 and (from two observer warps) when step commits complete and ring loads land.
+--backward traces the backward pass's dQ and dK/dV kernels (CTAs of head 0,
+sequence 0): per key block (dQ) or query block (dK/dV) the gradient math, the
+waits between blocks and how late the MMA-issuing threads see each hand-off.
 """
 from __future__ import annotations
 
@@ -335,6 +338,94 @@ def summarize_persistent(a: np.ndarray, ob: np.ndarray) -> dict:
     return res
 
 
+def run_backward(w: wl.Workload, repeats: int = 3, flags=()):
+    """Stamps of the backward kernels' last launch: ([query blocks, 1024],
+    [key blocks, 1024]) for the dQ and dK/dV kernels."""
+    from . import binding
+
+    load_trace_lib(flags)
+    L = binding.open_library(TRACE_LIB)  # with the C ABI's argument types
+    L.fmha_debug_set_bwd_trace.restype = ctypes.c_int
+    L.fmha_debug_set_bwd_trace.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    dev = torch.device("cuda:0")
+    inp = wl.make_inputs(w, seed=0)
+    dout = wl.make_dout(w, seed=0)
+    q, k, v, g = (t.to(dev) for t in (inp.q, inp.k, inp.v, dout))
+    cq = None if inp.cu_seqlens_q is None else inp.cu_seqlens_q.to(dev)
+    ck = None if inp.cu_seqlens_k is None else inp.cu_seqlens_k.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.heads, w.total_q), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(binding.fmha_bwd_workspace_size(w.heads, w.total_q) // 4, dtype=torch.float32, device=dev)
+    tq = torch.zeros(((w.max_seqlen_q + 127) // 128, 1024), dtype=torch.int64, device=dev)
+    tk = torch.zeros(((w.max_seqlen_k + 127) // 128, 1024), dtype=torch.int64, device=dev)
+    st = torch.cuda.current_stream()
+    rc = binding.fmha_fwd_gqa(q, k, v, out, lse, cq, ck, w.batch, w.total_q, w.total_k, w.max_seqlen_q,
+                              w.max_seqlen_k, w.heads, w.n_kv_heads, w.head_dim, w.softmax_scale, int(w.causal), st,
+                              library=L)
+    if rc != 0:
+        raise RuntimeError(f"fmha_fwd_gqa returned {rc}")
+    for _ in range(repeats):
+        L.fmha_debug_set_bwd_trace(ctypes.c_void_p(tq.data_ptr()), ctypes.c_void_p(tk.data_ptr()))
+        rc = binding.fmha_bwd(q, k, v, out, g, lse, dq, dk, dv, ws, cq, ck, w.batch, w.total_q, w.total_k,
+                              w.max_seqlen_q, w.max_seqlen_k, w.heads, w.n_kv_heads, w.head_dim, w.softmax_scale,
+                              int(w.causal), st, library=L)
+        if rc != 0:
+            raise RuntimeError(f"fmha_bwd returned {rc}")
+        torch.cuda.synchronize()
+    L.fmha_debug_set_bwd_trace(None, None)
+    return tq.cpu().numpy(), tk.cpu().numpy()
+
+
+def summarize_backward(a: np.ndarray, bk: np.ndarray) -> dict:
+    """Medians over steady-state blocks (the 3rd to the 3rd-last of each CTA), SM cycles.
+
+    dQ kernel, per key block j (slots 8 j + e): 0 S and dP ready for the
+    gradient warps, 1 dP read and released to the dP issuer, 2 dS stored,
+    3 the dP issuer saw that release, 4 the S/dQ issuer saw dS, 5 the S/dQ
+    issuer, after issuing dQ(j), saw K of block j + 2, 6 the dP issuer saw V
+    of block j + 1.  dK/dV kernel, per query block
+    (item) it: 0 stage ready, 1 / 3 half 0 / 1 scores ready, 2 / 4 half 0 / 1
+    P stored, 5 / 6 dV issuer saw half 0 / 1, 7 producer passed the stage's
+    release; set-up at 1000 (entry) and 1001 (roles start)."""
+    med = lambda v: float(np.median(v)) if len(v) else None  # noqa: E731
+    d = {k: [] for k in ("period", "math", "wait_between_blocks", "dp_release_seen", "ds_seen", "setup")}
+    for row in a:
+        if row[1000] == 0:
+            continue
+        d["setup"].append(row[1001] - row[1000])
+        n = 0
+        while n < 64 and row[8 * n] != 0:
+            n += 1
+        for j in range(2, n - 2):
+            s0, s1, s2, s3, s4 = (int(row[8 * j + e]) for e in range(5))
+            d["period"].append(int(row[8 * (j + 1)]) - s0)
+            d["math"].append(s2 - s0)
+            d["wait_between_blocks"].append(int(row[8 * (j + 1)]) - s2)
+            d["dp_release_seen"].append(s3 - s1)
+            d["ds_seen"].append(s4 - s2)
+    res = {"dq": {k: med(v) for k, v in d.items()}}
+    d = {k: [] for k in ("period", "math_h0", "math_h1", "wait_h0", "wait_h1", "p0_seen", "p1_seen", "setup")}
+    for row in bk:
+        if row[1000] == 0:
+            continue
+        d["setup"].append(row[1001] - row[1000])
+        n = 0
+        while n < 64 and row[8 * n] != 0:
+            n += 1
+        for it in range(2, n - 2):
+            e = [int(row[8 * it + x]) for x in range(8)]
+            d["period"].append(int(row[8 * (it + 1) + 1]) - e[1])
+            d["math_h0"].append(e[2] - e[1])
+            d["math_h1"].append(e[4] - e[3])
+            d["wait_h0"].append(int(row[8 * (it + 1) + 1]) - e[4])
+            d["wait_h1"].append(e[3] - e[2])
+            d["p0_seen"].append(e[5] - e[2])
+            d["p1_seen"].append(e[6] - e[4])
+    res["dkdv"] = {k: med(v) for k, v in d.items()}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default=wl.C2.name, choices=sorted(wl.CONFIGS))
@@ -343,8 +434,13 @@ def main():
     ap.add_argument("--flags", default="", help="extra -D flags for the trace build (tuning variants)")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush before each launch")
     ap.add_argument("--persistent", action="store_true", help="trace the persistent variant")
+    ap.add_argument("--backward", action="store_true", help="trace the backward pass's dQ and dK/dV kernels")
     args = ap.parse_args()
     w = wl.CONFIGS[args.workload]
+    if args.backward:
+        a, bk = run_backward(w, flags=args.flags.split())
+        print(json.dumps({"workload": w.name, "flags": args.flags, "backward": summarize_backward(a, bk)}, indent=1))
+        return
     if args.persistent:
         a, ob = run_persistent(w, flags=args.flags.split())
         print(json.dumps({"workload": w.name, "flags": args.flags, "persistent": summarize_persistent(a, ob)}, indent=1))
