@@ -154,6 +154,40 @@ int launch_persistent(fmha::FwdParams& p, int ctas, fmha_stream_t stream) {
   return cudaGetLastError() == cudaSuccess ? FMHA_OK : FMHA_ERR_CUDA;
 }
 
+// The backward pass's dK/dV kernel runs on a second stream of the library's,
+// forked from the caller's stream once D is written and joined back before
+// the call returns, so that the dQ and dK/dV CTAs fill each other's last
+// waves (when one sequence's K/V fits in L2).  One stream and two events per device, created on first use; the
+// fork, the launch and the join are made under a lock, so that calls from
+// several host threads do not interleave their event records.  A stream
+// capture follows the fork and the join (the second stream joins the capture
+// through the first event).  -DFMHA_BWD_FORK=0 runs both on the caller's stream.
+#ifndef FMHA_BWD_FORK
+#define FMHA_BWD_FORK 1
+#endif
+struct BwdFork {
+  cudaStream_t aux = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool ready = false;
+};
+std::mutex g_bwd_fork_mu;
+
+// this device's fork objects (under g_bwd_fork_mu), or nullptr
+BwdFork* bwd_fork_locked() {
+  static BwdFork forks[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  BwdFork& f = forks[dev];
+  if (!f.ready) {
+    if (cudaStreamCreateWithFlags(&f.aux, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+    f.ready = true;
+  }
+  return &f;
+}
+
 // e4m3 V^T [rows, kpad] bytes (keys contiguous), box 128 keys x 128 rows, 128B swizzle.
 bool make_map_vt(CUtensorMap* m, const void* ptr, int64_t rows, int64_t kpad) {
   auto fn = encode_fn();
@@ -446,16 +480,32 @@ extern "C" int fmha_bwd(const void* q, const void* k, const void* v, const void*
     fmha::bwd::fmha_bwd_dot_kernel<<<static_cast<unsigned>(blocks), fmha::bwd::kDotThreads, 0, st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
   }
-  if (qblocks > 0 && total_q > 0) {
+  const bool run_dq = qblocks > 0 && total_q > 0, run_dkdv = kblocks > 0 && total_k > 0;
+  std::unique_lock<std::mutex> lock(g_bwd_fork_mu, std::defer_lock);
+  BwdFork* fork = nullptr;
+  // (a sequence whose K/V exceeds L2 keeps both kernels on the caller's stream:
+  // run at once, their CTAs would split L2 between two working sets)
+  const bool kv_fits_l2 = static_cast<int64_t>(kv_heads) * max_seqlen_k * head_dim * 4 <= kL2GroupBytes;
+  if (FMHA_BWD_FORK && run_dq && run_dkdv && kv_fits_l2) {
+    lock.lock();
+    fork = bwd_fork_locked();
+    if (fork != nullptr && (cudaEventRecord(fork->fork, st) != cudaSuccess ||
+                            cudaStreamWaitEvent(fork->aux, fork->fork, 0) != cudaSuccess))
+      return FMHA_ERR_CUDA;
+  }
+  if (run_dq) {
     fmha::bwd::fmha_bwd_dq_kernel<<<dim3(heads, qblocks, batch), fmha::bwd::kDqThreads, fmha::bwd::DqSmem::kBytes,
                                     st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
   }
-  if (kblocks > 0 && total_k > 0) {
+  if (run_dkdv) {
     fmha::bwd::fmha_bwd_dkdv_kernel<<<dim3(kv_heads, kblocks, batch), fmha::bwd::kDkvThreads,
-                                      fmha::bwd::DkvSmem::kBytes, st>>>(p);
+                                      fmha::bwd::DkvSmem::kBytes, fork != nullptr ? fork->aux : st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FMHA_ERR_CUDA;
   }
+  if (fork != nullptr &&
+      (cudaEventRecord(fork->join, fork->aux) != cudaSuccess || cudaStreamWaitEvent(st, fork->join, 0) != cudaSuccess))
+    return FMHA_ERR_CUDA;
   return FMHA_OK;
 }
 

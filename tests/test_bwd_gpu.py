@@ -188,3 +188,65 @@ def test_backward_deterministic():
     for _ in range(4):
         again = run_fwd_bwd(inp, dO)
         assert all(torch.equal(a, b) for a, b in zip(first, again))
+
+
+def test_backward_cuda_graph_and_no_fork():
+    # The call forks the dK/dV kernel onto a second stream of the library's and
+    # joins it back before returning: a CUDA graph captured from the caller's
+    # stream replays all three kernels (inputs overwritten in place between
+    # replays), and the results equal those of a build that runs every kernel
+    # on the caller's stream (-DFMHA_BWD_FORK=0).
+    import os
+
+    from attention_forward_mbarrier_gb300 import build as _build
+
+    w = wl.varlen("bwd_graph", (700, 300, 129), 4, causal=True, kv_heads=2)
+    first, second = (wl.make_inputs(w, seed=s) for s in (53, 54))
+    douts = [wl.make_dout(w, seed=s) for s in (53, 54)]
+    dev = torch.device("cuda:0")
+    q, k, v, g = (t.to(dev) for t in (first.q, first.k, first.v, douts[0]))
+    cu = first.cu_seqlens_q.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.heads, w.total_q), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(binding.fmha_bwd_workspace_size(w.heads, w.total_q) // 4, dtype=torch.float32, device=dev)
+
+    def call(stream, library=None):
+        assert binding.fmha_fwd_gqa(q, k, v, out, lse, cu, cu, w.batch, w.total_q, w.total_k, w.max_seqlen_q,
+                                    w.max_seqlen_k, w.heads, w.n_kv_heads, w.head_dim, w.softmax_scale, 1,
+                                    stream, library=library) == binding.FMHA_OK
+        assert binding.fmha_bwd(q, k, v, out, g, lse, dq, dk, dv, ws, cu, cu, w.batch, w.total_q, w.total_k,
+                                w.max_seqlen_q, w.max_seqlen_k, w.heads, w.n_kv_heads, w.head_dim,
+                                w.softmax_scale, 1, stream, library=library) == binding.FMHA_OK
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # first calls outside the capture (per-process set-up)
+        call(side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call(torch.cuda.current_stream())
+    path = os.path.join(_build.PKG, "libfmha_nofork.so")
+    _build.build(force=True, extra_flags=["-DFMHA_BWD_FORK=0"], out=path)
+    serial = binding.open_library(path)
+    for inp, dO in zip((first, second), douts):
+        q.copy_(inp.q.to(dev))
+        k.copy_(inp.k.to(dev))
+        v.copy_(inp.v.to(dev))
+        g.copy_(dO.to(dev))
+        for t in (dq, dk, dv):
+            t.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        got = (dq.clone(), dk.clone(), dv.clone())
+        call(torch.cuda.current_stream(), library=serial)
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(got, (dq, dk, dv)))
+        rq, rk, rv = oracle.oracle_bwd(inp.q, inp.k, inp.v, dO, *inp.oracle_args()[3:])
+        compare_grad(got[0].float().cpu().numpy(), rq, "dq")
+        compare_grad(got[1].float().cpu().numpy(), rk, "dk")
+        compare_grad(got[2].float().cpu().numpy(), rv, "dv")
+    st, detail = binding.fmha_get_device_status(library=serial)
+    assert st == binding.FMHA_OK, (st, detail)
