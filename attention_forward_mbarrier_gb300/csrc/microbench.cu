@@ -15,6 +15,12 @@
 //   uniform  1 = the whole warp runs the loop and one lane issues through a
 //              predicate (warp-uniform operands); 0 = lane 0 inside a branch
 // fmha_microbench_tmem_ld: tcgen05.ld 32x32b.x32 + wait, 4 warps.
+// fmha_microbench_mma_mix / _boundary / _handoff / _pingpong: the attention
+//   kernel's MMA stream, the issuing thread's cost at a step boundary,
+//   barrier hand-off latency while MMAs run, and two alternating issuers
+//   (each documented at its kernel below).
+// fmha_microbench_empty_launch: an empty one-wave kernel, for the launch
+//   envelope inside a pair of timing events.
 // Each writes the per-CTA cycle count of its timed region to out_cycles
 // (host memory, n_ctas entries) and returns 0, 1 on a bad argument, 2 on a
 // CUDA error, 3 if a completion wait expired (bounded at 1 s).
@@ -344,6 +350,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) mma_probe(int issuers, int reps
 // mbarrier.try_wait on an already-completed barrier; 1: the try_wait alone;
 // 2: the commit alone.  Modes 3-5: the same three after 16 MMAs of N=256
 // (128 cycles each, so more work is still in flight at the boundary).
+// Mode 6: mode 0 while warps 1-3 poll (try_wait, every lane) a barrier that
+// never completes; 7: mode 0 while warps 1-3 wait for each commit's phase of
+// the committed barrier (as softmax warps wait for S); 8: the commit then a
+// dependent shared-memory load instead of the try_wait.
 // Returns the summed cycles of that boundary sequence.
 template <int mode>
 __global__ void __launch_bounds__(kTcThreads, 1) boundary_probe(int reps, long long* out, int* status) {
@@ -353,8 +363,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) boundary_probe(int reps, long l
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t tmem = tc_setup(smem, base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile uint32_t* done_flag = reinterpret_cast<volatile uint32_t*>(smem + kMbBar + 96);
+  if (threadIdx.x == 0) *done_flag = 0u;
+  __syncthreads();
   long long acc = 0;
-  if (warp == 0 && lane == 0) {
+  if (mode == 6 && warp > 0) {
+    const uint64_t g0 = ptx::globaltimer_ns();
+    while (*done_flag == 0u && ptx::globaltimer_ns() - g0 < 1000000000ull)
+      if (ptx::mbar_try_wait(base + kMbBar + 16u, 0)) status[0] = 1;  // never completes
+  } else if (mode == 7 && warp > 0) {
+    for (int r = 0; r < reps; ++r) {
+      const uint64_t g0 = ptx::globaltimer_ns();
+      bool ok = true;
+      while (!ptx::mbar_try_wait(base + kMbBar + 8u, static_cast<uint32_t>(r & 1)))
+        if (ptx::globaltimer_ns() - g0 > 1000000000ull) {
+          ok = false;
+          break;
+        }
+      if (!ok) {
+        status[0] = 1;
+        break;
+      }
+    }
+  } else if (warp == 0 && lane == 0) {
     const uint32_t done_bar = base + kMbBar + 24u;
     ptx::mbar_arrive(done_bar);  // count 1: phase 0 completes now
     const uint32_t id_qk = ptx::idesc_bf16_f32(128, 128, false, false);
@@ -386,13 +417,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) boundary_probe(int reps, long l
       long long a, b;
       asm volatile("mov.u64 %0, %%clock64;" : "=l"(a)::"memory");
       if (mode != 1 && mode != 4) ptx::mma_commit(base + kMbBar + 8u);
-      if (mode != 2 && mode != 5 && !ptx::mbar_try_wait(done_bar, 0)) ++fails;
+      if (mode == 8) {
+        if (*done_flag != 0u) ++fails;
+      } else if (mode != 2 && mode != 5 && !ptx::mbar_try_wait(done_bar, 0)) {
+        ++fails;
+      }
       asm volatile("mov.u64 %0, %%clock64;" : "=l"(b)::"memory");
       acc += b - a;
     }
     const uint32_t bar = base + kMbBar;
     ptx::mma_commit(bar);
     if (!bounded_wait(bar) || fails) status[0] = 1;
+    *done_flag = 1u;
   }
   __syncwarp();
   tc_teardown(tmem);
@@ -411,12 +447,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) boundary_probe(int reps, long l
 // 6: the two-tile stream with a tcgen05.commit after every 8 MMAs (as the
 // kernel signals S ready and frees ring slots); 7: a commit after every MMA;
 // 8: one commit per 32 MMAs; 9: tile 0's QK^T only, a commit after every 8.
+// 10: the stream of mode 0 on random operands (bf16 of magnitude [0.5, 4)
+// and random sign in Q, K and V, so S and P are random too) instead of zeros;
+// 11: mode 1 on random operands.
 // In-loop commits go to a barrier nobody waits on.  P and S share columns
 // exactly as in the kernel (the next QK^T of a tile follows its PV).
 template <int mode>
 __global__ void __launch_bounds__(kTcThreads, 1) mma_mix_probe(int reps, long long* out, int* status) {
   constexpr int n_tiles = (mode == 4 || mode == 5 || mode == 9) ? 1 : 2;
-  constexpr bool do_pv = mode != 1 && mode != 9;
+  constexpr bool do_pv = mode != 1 && mode != 9 && mode != 11;
   constexpr bool do_qk = mode != 2;
   constexpr bool commit_group = mode == 6 || mode == 9;
   extern __shared__ uint8_t smem_raw[];
@@ -424,6 +463,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) mma_mix_probe(int reps, long lo
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t tmem = tc_setup(smem, base);
+  if constexpr (mode >= 10) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(smem);
+    for (uint32_t i = threadIdx.x; i < kMbBar / 4; i += kTcThreads) {
+      uint32_t h = i * 2654435761u + 0x9e3779b9u;
+      h ^= h >> 15;
+      h *= 2246822519u;
+      h ^= h >> 13;
+      const uint32_t lo = (h & 0x8000u) | ((126u + (h >> 4) % 3u) << 7) | (h & 0x7Fu);
+      const uint32_t hi = ((h >> 16) & 0x8000u) | ((126u + (h >> 20) % 3u) << 7) | ((h >> 8) & 0x7Fu);
+      w[i] = lo | (hi << 16);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+  }
   volatile uint32_t* done_flag = reinterpret_cast<volatile uint32_t*>(smem + kMbBar + 96);
   if (threadIdx.x == 0) *done_flag = 0u;
   __syncthreads();
@@ -494,6 +547,230 @@ __global__ void __launch_bounds__(kTcThreads, 1) mma_mix_probe(int reps, long lo
   __syncwarp();
   tc_teardown(tmem);
   if (threadIdx.x == 0) out[blockIdx.x] = t1 - t0;
+}
+
+// Hand-off latency while an MMA stream runs.  Warp 0 (one lane) issues MMAs
+// until the measuring warps are done: mode 0 none, 1 QK^T-like (A and B in
+// shared memory, N = 128), 2 PV-like (A = P in tensor memory, B = V in shared
+// memory, N = 128), 3 the attention stream (per tile 8 PV then 8 QK^T, two
+// tiles).  what 0: warps 1 and 2 (one lane each) ping-pong `rounds` times
+// through two count-1 mbarriers (arrive, the other side polls with
+// try_wait); out = summed round-trip cycles.  what 1: warp 1 chases a
+// pointer through shared memory `rounds` times (dependent ld.shared); out =
+// summed cycles.  what 2: the ping-pong of what 0 through two named barriers
+// (bar.arrive / bar.sync, whole warps; both sides run all rounds, so every
+// bar.sync is matched).  Every mbarrier or flag wait is bounded (1 s, status 1).
+template <int mode>
+__global__ void __launch_bounds__(kTcThreads, 1) handoff_probe(int what, int rounds, long long* out, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t tmem = tc_setup(smem, base);
+  volatile uint32_t* started = reinterpret_cast<volatile uint32_t*>(smem + kMbBar + 96);
+  volatile uint32_t* done_flag = reinterpret_cast<volatile uint32_t*>(smem + kMbBar + 100);
+  uint32_t* chain = reinterpret_cast<uint32_t*>(smem + kMbBar + 128);  // 256 words, in the extra 32 KiB
+  if (threadIdx.x == 0) {
+    *started = 0u;
+    *done_flag = 0u;
+  }
+  for (int i = threadIdx.x; i < 256; i += kTcThreads) chain[i] = static_cast<uint32_t>((i * 97 + 13) & 255);
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar_x = base + kMbBar + 16u, bar_y = base + kMbBar + 24u;
+  auto wait_parity = [&](uint32_t bar, uint32_t parity) {
+    const uint64_t g0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity))
+      if (ptx::globaltimer_ns() - g0 > 1000000000ull) return false;
+    return true;
+  };
+  auto wait_flag = [&](volatile uint32_t* f) {
+    const uint64_t g0 = ptx::globaltimer_ns();
+    while (*f == 0u)
+      if (ptx::globaltimer_ns() - g0 > 1000000000ull) return false;
+    return true;
+  };
+  long long acc = 0;
+  if (warp == 0 && lane == 0) {
+    const uint32_t id_qk = ptx::idesc_bf16_f32(128, 128, false, false);
+    const uint32_t id_pv = ptx::idesc_bf16_f32(128, 128, false, true);
+    const uint64_t q0 = ptx::smem_desc_sw128(base + kMbA, 16, 1024);
+    const uint64_t k0 = ptx::smem_desc_sw128(base + kMbB, 16, 1024);
+    const uint64_t v0 = ptx::smem_desc_sw128(base + kMbB + 32768u, 16384, 1024);
+    bool any = false;
+    const uint64_t g0 = ptx::globaltimer_ns();
+    for (int r = 0; r < (1 << 16) && *done_flag == 0u; ++r) {
+      if constexpr (mode == 0) {
+        *started = 1u;
+        if (ptx::globaltimer_ns() - g0 > 1000000000ull) break;
+        continue;
+      } else {
+#pragma unroll
+        for (int tl = 0; tl < (mode == 3 ? 2 : 1); ++tl) {
+          if (mode == 2 || mode == 3) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              ptx::mma_ts_leader(tmem + 256u + 128u * tl, tmem + 128u * tl + 8u * k, v0 + ((2048u * k) >> 4), id_pv, 1u,
+                                 1u);
+          }
+          if (mode == 1 || mode == 3) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t off = ((k >> 2) * 16384u + (k & 3) * 32u) >> 4;
+              ptx::mma_ss_leader(tmem + 128u * tl, q0 + off, k0 + off, id_qk, k > 0 ? 1u : 0u, 1u);
+            }
+          }
+        }
+        any = true;
+        if (r == 1) *started = 1u;
+      }
+    }
+    *started = 1u;
+    if (any) {
+      const uint32_t bar = base + kMbBar;
+      ptx::mma_commit_leader(bar, 1u);
+      if (!bounded_wait(bar)) status[0] = 1;
+    }
+  } else if (warp == 1 && what == 2) {
+    if (!wait_flag(started)) status[0] = 1;
+    __syncwarp();
+    for (int r = 0; r < rounds; ++r) {
+      long long a, b;
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(a)::"memory");
+      asm volatile("bar.arrive 1, 64;" ::: "memory");
+      asm volatile("bar.sync 2, 64;" ::: "memory");
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(b)::"memory");
+      acc += b - a;
+    }
+    if (lane == 0) *done_flag = 1u;
+  } else if (warp == 2 && what == 2) {
+    for (int r = 0; r < rounds; ++r) {
+      asm volatile("bar.sync 1, 64;" ::: "memory");
+      asm volatile("bar.arrive 2, 64;" ::: "memory");
+    }
+  } else if (warp == 1 && lane == 0) {
+    if (!wait_flag(started)) status[0] = 1;
+    if (what == 0) {
+      for (int r = 0; r < rounds; ++r) {
+        long long a, b;
+        asm volatile("mov.u64 %0, %%clock64;" : "=l"(a)::"memory");
+        ptx::mbar_arrive(bar_x);
+        const bool ok = wait_parity(bar_y, static_cast<uint32_t>(r & 1));
+        asm volatile("mov.u64 %0, %%clock64;" : "=l"(b)::"memory");
+        if (!ok) {
+          status[0] = 1;
+          break;
+        }
+        acc += b - a;
+      }
+    } else {
+      uint32_t i = 0;
+      long long a, b;
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(a)::"memory");
+      for (int r = 0; r < rounds; ++r) i = reinterpret_cast<volatile uint32_t*>(chain)[i];
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(b)::"memory");
+      acc = b - a;
+      if (i == 12345u) status[1] = 1;  // keeps the chain
+    }
+    *done_flag = 1u;
+  } else if (warp == 2 && lane == 0 && what == 0) {
+    for (int r = 0; r < rounds; ++r) {
+      if (!wait_parity(bar_x, static_cast<uint32_t>(r & 1))) {
+        status[0] = 1;
+        break;
+      }
+      ptx::mbar_arrive(bar_y);
+    }
+  }
+  __syncwarp();
+  tc_teardown(tmem);
+  if (threadIdx.x == 32) out[blockIdx.x] = acc;
+}
+
+// Two issuing threads alternating MMA groups.  Each round is one KV step of
+// the attention stream: tile 0's group (8 PV into O_0, then 8 QK^T into S_0)
+// and tile 1's group.  variant 0: one thread issues both groups with a
+// commit after each (the attention kernel's schedule); 1: tile t's group is
+// issued by warp t, which then commits and hands a token (a count-1
+// mbarrier) to the other issuer, which waits for it before its group; 2: as
+// 1 with the token handed over before the commit; 3: as 1 without commits.
+// out = cycles of `reps` rounds (32 MMAs each) on the thread that issues the
+// last group.  Every wait is bounded (1 s, status 1).
+template <int variant>
+__global__ void __launch_bounds__(kTcThreads, 1) pingpong_probe(int reps, long long* out, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t tmem = tc_setup(smem, base);
+  const uint32_t tok[2] = {base + kMbBar + 32u, base + kMbBar + 40u};
+  const uint32_t spare[2] = {base + kMbBar + 48u, base + kMbBar + 56u};
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(tok[i], 1);
+      ptx::mbar_init(spare[i], 1);
+    }
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t id_qk = ptx::idesc_bf16_f32(128, 128, false, false);
+  const uint32_t id_pv = ptx::idesc_bf16_f32(128, 128, false, true);
+  const uint64_t q0 = ptx::smem_desc_sw128(base + kMbA, 16, 1024);
+  const uint64_t k0 = ptx::smem_desc_sw128(base + kMbB, 16, 1024);
+  const uint64_t v0 = ptx::smem_desc_sw128(base + kMbB + 32768u, 16384, 1024);
+  auto group = [&](int tl) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      ptx::mma_ts(tmem + 256u + 128u * tl, tmem + 128u * tl + 8u * k, v0 + ((2048u * k) >> 4), id_pv, 1u);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint64_t off = ((k >> 2) * 16384u + (k & 3) * 32u) >> 4;
+      ptx::mma_ss(tmem + 128u * tl, q0 + off, k0 + off, id_qk, k > 0 ? 1u : 0u);
+    }
+  };
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    const uint64_t g0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity))
+      if (ptx::globaltimer_ns() - g0 > 1000000000ull) return false;
+    return true;
+  };
+  long long t0 = 0, t1 = 0;
+  if (variant == 0 && warp == 0 && lane == 0) {
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0)::"memory");
+    for (int r = 0; r < reps; ++r) {
+      group(0);
+      ptx::mma_commit(spare[0]);
+      group(1);
+      ptx::mma_commit(spare[1]);
+    }
+    ptx::mma_commit(base + kMbBar);
+    if (!bounded_wait(base + kMbBar)) status[0] = 1;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1)::"memory");
+  } else if (variant > 0 && warp < 2 && lane == 0) {
+    const int me = warp;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0)::"memory");
+    for (int r = 0; r < reps; ++r) {
+      // tile 0 at round r follows tile 1's group of round r - 1; tile 1 follows tile 0's of round r
+      bool ok = true;
+      if (me == 0 && r > 0) ok = wait(tok[0], static_cast<uint32_t>((r - 1) & 1));
+      if (me == 1) ok = wait(tok[1], static_cast<uint32_t>(r & 1));
+      if (!ok) {
+        status[0] = 1;
+        break;
+      }
+      group(me);
+      if (variant == 1) ptx::mma_commit(spare[me]);
+      ptx::mbar_arrive(tok[1 - me]);
+      if (variant == 2) ptx::mma_commit(spare[me]);
+    }
+    ptx::mma_commit(base + kMbBar + 8u * me);
+    if (!bounded_wait(base + kMbBar + 8u * me)) status[0] = 1;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1)::"memory");
+  }
+  __syncwarp();
+  tc_teardown(tmem);
+  if (threadIdx.x == (variant == 0 ? 0 : 32)) out[blockIdx.x] = t1 - t0;
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) tmem_ld_probe(int reps, long long* out, int* status) {
@@ -634,7 +911,7 @@ extern "C" int fmha_microbench_mma(int a_tmem, int b_mn, int n, int issuers, int
 // Cycles of `reps` rounds of the attention MMA stream (32 MMAs a round) in
 // the given mode of mma_mix_probe.  Returns as fmha_microbench_mma.
 extern "C" int fmha_microbench_mma_mix(int mode, int reps, long long* out_cycles, int n_ctas) {
-  if (mode < 0 || mode > 9 || reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
+  if (mode < 0 || mode > 11 || reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
   long long* d_out = nullptr;
   int* d_status = nullptr;
   if (!alloc(&d_out, &d_status, n_ctas)) return 2;
@@ -653,7 +930,69 @@ extern "C" int fmha_microbench_mma_mix(int mode, int reps, long long* out_cycles
     case 6: launch(mma_mix_probe<6>); break;
     case 7: launch(mma_mix_probe<7>); break;
     case 8: launch(mma_mix_probe<8>); break;
-    default: launch(mma_mix_probe<9>); break;
+    case 9: launch(mma_mix_probe<9>); break;
+    case 10: launch(mma_mix_probe<10>); break;
+    default: launch(mma_mix_probe<11>); break;
+  }
+  return finish(d_out, d_status, nullptr, out_cycles, n_ctas);
+}
+
+// Summed cycles of handoff_probe (mode: the MMA stream; what: 0 mbarrier
+// ping-pong round trips, 1 dependent shared-memory loads, 2 named-barrier
+// ping-pong round trips) over `rounds`.  Returns as
+// fmha_microbench_mma.
+extern "C" int fmha_microbench_handoff(int mode, int what, int rounds, long long* out_cycles, int n_ctas) {
+  if (mode < 0 || mode > 3 || what < 0 || what > 2 || rounds < 1 || rounds > (1 << 20) || n_ctas < 1 ||
+      out_cycles == nullptr)
+    return 1;
+  long long* d_out = nullptr;
+  int* d_status = nullptr;
+  if (!alloc(&d_out, &d_status, n_ctas)) return 2;
+  const int smem = static_cast<int>(kMbSmem) + 32768;
+  auto launch = [&](auto kernel) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    kernel<<<n_ctas, kTcThreads, smem>>>(what, rounds, d_out, d_status);
+  };
+  switch (mode) {
+    case 0: launch(handoff_probe<0>); break;
+    case 1: launch(handoff_probe<1>); break;
+    case 2: launch(handoff_probe<2>); break;
+    default: launch(handoff_probe<3>); break;
+  }
+  return finish(d_out, d_status, nullptr, out_cycles, n_ctas);
+}
+
+namespace {
+__global__ void __launch_bounds__(512, 1) empty_probe() {}
+}  // namespace
+
+// Launches an empty kernel of `grid` CTAs of `block` threads with `smem`
+// bytes of dynamic shared memory on `stream` (asynchronous): the launch
+// envelope a one-wave kernel pays inside a pair of timing events.  Returns 0,
+// 1 on a bad argument, 2 on a launch error.
+extern "C" int fmha_microbench_empty_launch(int grid, int block, int smem, void* stream) {
+  if (grid < 1 || block < 32 || block > 512 || smem < 0 || smem > 232448) return 1;
+  if (cudaFuncSetAttribute(empty_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 2;
+  empty_probe<<<grid, block, smem, static_cast<cudaStream_t>(stream)>>>();
+  return cudaGetLastError() == cudaSuccess ? 0 : 2;
+}
+
+// Cycles of `reps` rounds of pingpong_probe<variant>.  Returns as
+// fmha_microbench_mma.
+extern "C" int fmha_microbench_pingpong(int variant, int reps, long long* out_cycles, int n_ctas) {
+  if (variant < 0 || variant > 3 || reps < 1 || reps > (1 << 20) || n_ctas < 1 || out_cycles == nullptr) return 1;
+  long long* d_out = nullptr;
+  int* d_status = nullptr;
+  if (!alloc(&d_out, &d_status, n_ctas)) return 2;
+  auto launch = [&](auto kernel) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMbSmem));
+    kernel<<<n_ctas, kTcThreads, kMbSmem>>>(reps, d_out, d_status);
+  };
+  switch (variant) {
+    case 0: launch(pingpong_probe<0>); break;
+    case 1: launch(pingpong_probe<1>); break;
+    case 2: launch(pingpong_probe<2>); break;
+    default: launch(pingpong_probe<3>); break;
   }
   return finish(d_out, d_status, nullptr, out_cycles, n_ctas);
 }
@@ -661,7 +1000,7 @@ extern "C" int fmha_microbench_mma_mix(int mode, int reps, long long* out_cycles
 // Summed cycles of the step-boundary sequence of boundary_probe over `reps`
 // rounds.  Returns as fmha_microbench_mma.
 extern "C" int fmha_microbench_boundary(int mode, int reps, long long* out_cycles, int n_ctas) {
-  if (mode < 0 || mode > 5 || reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
+  if (mode < 0 || mode > 8 || reps < 1 || n_ctas < 1 || out_cycles == nullptr) return 1;
   long long* d_out = nullptr;
   int* d_status = nullptr;
   if (!alloc(&d_out, &d_status, n_ctas)) return 2;
@@ -675,7 +1014,10 @@ extern "C" int fmha_microbench_boundary(int mode, int reps, long long* out_cycle
     case 2: launch(boundary_probe<2>); break;
     case 3: launch(boundary_probe<3>); break;
     case 4: launch(boundary_probe<4>); break;
-    default: launch(boundary_probe<5>); break;
+    case 5: launch(boundary_probe<5>); break;
+    case 6: launch(boundary_probe<6>); break;
+    case 7: launch(boundary_probe<7>); break;
+    default: launch(boundary_probe<8>); break;
   }
   return finish(d_out, d_status, nullptr, out_cycles, n_ctas);
 }

@@ -44,9 +44,46 @@ def load():
     F = ctypes.POINTER(ctypes.c_float)
     L.fmha_probe_exp2_poly.restype = ctypes.c_int
     L.fmha_probe_exp2_poly.argtypes = [F, F, F, ctypes.c_int]
+    L.fmha_microbench_empty_launch.restype = ctypes.c_int
+    L.fmha_microbench_empty_launch.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p]
+    L.fmha_microbench_pingpong.restype = ctypes.c_int
+    L.fmha_microbench_pingpong.argtypes = [ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
+    L.fmha_microbench_handoff.restype = ctypes.c_int
+    L.fmha_microbench_handoff.argtypes = [ctypes.c_int] * 3 + [P, ctypes.c_int]
     L.fmha_microbench_tmem_ld.restype = ctypes.c_int
     L.fmha_microbench_tmem_ld.argtypes = [ctypes.c_int, P, ctypes.c_int]
     return L
+
+
+def empty_launch_envelope(L, steps: int = 40) -> dict:
+    """Median microseconds between two CUDA events around the launch of an
+    empty kernel (144 CTAs of 512 threads, the dense workload's grid), after a
+    write-then-read pass over 2 x 504 MiB that flushes L2 and keeps the GPU
+    busy while the host enqueues, as the benchmark times its launches."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.current_stream(dev)
+    scratch = torch.empty(132 << 20, dtype=torch.float32, device=dev)
+    reader = torch.zeros(132 << 20, dtype=torch.float32, device=dev)
+    sink = torch.empty(1, dtype=torch.float32, device=dev)
+    res = {}
+    for smem_kb in (0, 200):
+        ms = []
+        for i in range(steps + 5):
+            scratch.zero_()
+            sink.copy_(reader.sum().reshape(1))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            rc = L.fmha_microbench_empty_launch(144, 512, smem_kb * 1024, ctypes.c_void_p(st.cuda_stream))
+            e1.record(st)
+            if rc != 0:
+                raise RuntimeError(f"empty launch failed with {rc}")
+            torch.cuda.synchronize()
+            if i >= 5:
+                ms.append(e0.elapsed_time(e1))
+        res[f"grid144_block512_smem{smem_kb}k"] = round(statistics.median(ms) * 1000, 2)
+    return res
 
 
 def exp2_poly_values(x):
@@ -124,7 +161,9 @@ def main():
                                   (2, "pv_only_two_tiles", 16), (3, "pv_then_qk_with_smem_writes", 32),
                                   (4, "one_tile_with_tmem_ld_st", 16), (5, "one_tile", 16),
                                   (6, "pv_then_qk_commit_every_8", 32), (7, "pv_then_qk_commit_every_mma", 32),
-                                  (8, "pv_then_qk_commit_every_32", 32), (9, "qk_one_tile_commit_every_8", 8)):
+                                  (8, "pv_then_qk_commit_every_32", 32), (9, "qk_one_tile_commit_every_8", 8),
+                                  (10, "pv_then_qk_two_tiles_random_operands", 32),
+                                  (11, "qk_only_two_tiles_random_operands", 16)):
         _median(L.fmha_microbench_mma_mix, mode, 8, n_ctas=sms)
         c1 = _median(L.fmha_microbench_mma_mix, mode, 64, n_ctas=sms)
         c2 = _median(L.fmha_microbench_mma_mix, mode, 192, n_ctas=sms)
@@ -133,10 +172,34 @@ def main():
     # issuing-thread cycles at a step boundary, after 16 MMAs in flight
     bnd = {}
     for mode, name in ((0, "commit_then_try_wait"), (1, "try_wait_only"), (2, "commit_only"),
-                       (3, "n256_commit_then_try_wait"), (4, "n256_try_wait_only"), (5, "n256_commit_only")):
+                       (3, "n256_commit_then_try_wait"), (4, "n256_try_wait_only"), (5, "n256_commit_only"),
+                       (6, "commit_then_try_wait_3_warps_polling_elsewhere"),
+                       (7, "commit_then_try_wait_3_warps_waiting_on_the_commit"),
+                       (8, "commit_then_shared_load")):
         _median(L.fmha_microbench_boundary, mode, 8, n_ctas=sms)
         bnd[name] = round(_median(L.fmha_microbench_boundary, mode, 128, n_ctas=sms) / 128, 1)
     out["step_boundary_cycles"] = bnd
+    # an mbarrier hand-off between two warps (half a ping-pong round trip) and
+    # a dependent shared-memory load, while the issuing warp runs MMA streams
+    hand = {}
+    for mode, name in ((0, "no_mma"), (1, "qk_like_ss_n128"), (2, "pv_like_ts_n128"), (3, "attention_stream")):
+        _median(L.fmha_microbench_handoff, mode, 0, 16, n_ctas=sms)
+        rt = _median(L.fmha_microbench_handoff, mode, 0, 256, n_ctas=sms)
+        ld = _median(L.fmha_microbench_handoff, mode, 1, 2048, n_ctas=sms)
+        nb = _median(L.fmha_microbench_handoff, mode, 2, 256, n_ctas=sms)
+        hand[name] = {"arrive_to_seen": round(rt / 256 / 2, 1), "ld_shared": round(ld / 2048, 1),
+                      "named_barrier_arrive_to_sync": round(nb / 256 / 2, 1)}
+    out["handoff_cycles_under_mma_stream"] = hand
+    # one issuer for both tiles' groups vs one issuer per tile passing a token
+    pp = {}
+    for variant, name in ((0, "one_issuer_commit_per_group"), (1, "two_issuers_commit_then_token"),
+                          (2, "two_issuers_token_then_commit"), (3, "two_issuers_token_no_commit")):
+        _median(L.fmha_microbench_pingpong, variant, 8, n_ctas=sms)
+        c1 = _median(L.fmha_microbench_pingpong, variant, 64, n_ctas=sms)
+        c2 = _median(L.fmha_microbench_pingpong, variant, 192, n_ctas=sms)
+        pp[name] = round((c2 - c1) / (128 * 32), 1)
+    out["alternating_issuers_cycles_per_mma"] = pp
+    out["empty_launch_us"] = empty_launch_envelope(L)
     _median(L.fmha_microbench_tmem_ld, 16, n_ctas=sms)
     cyc = _median(L.fmha_microbench_tmem_ld, reps, n_ctas=sms)
     out["tmem_ld_bytes_per_clk_per_sm"] = reps * 4 * 32 * 32 * 4 / cyc
