@@ -372,6 +372,16 @@ __device__ __forceinline__ float row_min128(const float (&s)[128]) {
   return ptx::fmin3(fminf(mn[0], mn[1]), mn[2], mn[3]);
 }
 
+// The lazy-rescale reference for a block: its row max (min for a negative
+// scale) replaces the reference in use m_used only when the scaled extreme
+// grew by more than `threshold` (log2 units); NaN while both are the mask
+// value compares false: keep.
+__device__ __forceinline__ float lazy_reference(const float (&s)[128], bool neg, float m_used, float c,
+                                                float threshold) {
+  const float m_blk = neg ? row_min128(s) : row_max128(s);
+  return (m_blk - m_used) * c > threshold ? m_blk : m_used;
+}
+
 // One softmax exp pass over a row of 128 scores with reference score m_ref
 // (the raw score whose scaled value is the row's largest): P = 2^(s c - m_ref c)
 // (one packed FMA per pair, ex2), bf16 pairs stored to TMEM at t_s (64
@@ -747,6 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
     const int row = m0 + kBlockM * t + r;  // sequence-local query index
     const int nb = n_blk(t);
     const float c = p.scale_log2;  // nonzero: the launcher passes 2^-126 for a zero scale
+    const float sum_limit = exp2f(p.rescale_threshold);  // row sums below it: every P below it
     // Softmax order is the order of s * c: for a negative scale the reference
     // score is the row minimum and masked scores hold +inf (s * c = -inf).
     const bool neg = c < 0.f;
@@ -773,18 +784,19 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         for (int k = 0; k < 128; ++k)
           if (k >= lim) s[k] = s_mask;
       }
-      // block max of s * c; the reference in use moves only when the scaled
-      // max grew by more than the threshold (lazy rescale; NaN while both are
-      // the mask value: keep)
-      float m_blk;
-      if (neg)
-        m_blk = row_min128(s);
-      else
-        m_blk = row_max128(s);
-      const float m_ref = (m_blk - m_used) * c > p.rescale_threshold ? m_blk : m_used;
+      // Reference score of this block (lazy rescale): the block max of s * c
+      // replaces the reference in use only when it grew by more than the
+      // threshold.  With one P hand-off in bf16 and two query tiles, after the
+      // row's first visible block the exponents are taken against the
+      // reference in use first, and the block max is found only when some
+      // row's sum exceeds 2^threshold: below that every P is below it too, so
+      // the rule keeps the reference and those P stand; above it the rule
+      // decides and, if it moves the reference, the pass is redone.
+      constexpr bool kStaleFirst = !kFp8 && kSplit == 4 && D::kTiles > 1;
+      bool stale = kStaleFirst && j > 0 && !__any_sync(0xffffffffu, isinf(m_used));
+      float m_ref = stale ? m_used : lazy_reference(s, neg, m_used, c, p.rescale_threshold);
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 2);
-      // an infinite m_used (nothing visible yet) gives alpha 0 (its O rows and l are still 0)
-      const float alpha = (m_ref == m_used) ? 1.f : ptx::ex2_approx((m_used - m_ref) * c);
+      float alpha = 1.f;
       // Rescale this warp's O rows.  PV_t(j-1) has completed (S_t(j) is
       // committed after it) and PV_t(j) waits for this warp's P hand-off (with
       // a split hand-off, the first one: hence the rescale before that signal).
@@ -808,14 +820,30 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVPart + t));
       };
       if constexpr (kFp8 && kSplit < 4) {
+        alpha = (m_ref == m_used) ? 1.f : ptx::ex2_approx((m_used - m_ref) * c);
         row_sum = exp_pass_fp8_split<kSplit>(s, c, m_ref, t_s, rescale_o, signal_part);
       } else if constexpr (kFp8) {
+        alpha = (m_ref == m_used) ? 1.f : ptx::ex2_approx((m_used - m_ref) * c);
         row_sum = exp_pass_fp8(s, c, m_ref, t_s);
         rescale_o();
       } else if constexpr (kSplit < 4) {
+        alpha = (m_ref == m_used) ? 1.f : ptx::ex2_approx((m_used - m_ref) * c);
         row_sum = exp_pass_split<kSplit>(s, c, m_ref, t_s, rescale_o, signal_part);
       } else {
-        row_sum = exp_pass(s, c, m_ref, t_s);
+        // head_dim 64: both passes inlined (measured faster there); else one copy
+        constexpr int kPassUnroll = HD == 64 ? 2 : 1;
+#pragma unroll kPassUnroll
+        for (int pass = 0; pass < 2; ++pass) {
+          row_sum = exp_pass(s, c, m_ref, t_s);
+          if (!stale || !__any_sync(0xffffffffu, row_sum > sum_limit)) break;
+          stale = false;
+          const float m_new = lazy_reference(s, neg, m_used, c, p.rescale_threshold);
+          if (!__any_sync(0xffffffffu, m_new != m_used)) break;
+          m_ref = m_new;
+          ptx::tmem_wait_st();  // the first pass's stores land before they are overwritten
+        }
+        // an infinite m_used (nothing visible yet) gives alpha 0 (its O rows and l are still 0)
+        alpha = (m_ref == m_used) ? 1.f : ptx::ex2_approx((m_used - m_ref) * c);
         rescale_o();
       }
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 3);

@@ -194,6 +194,29 @@ def test_uniform_inputs_wide_scores():
     check_full(wl.make_inputs(w, seed=5))
 
 
+@pytest.mark.parametrize("head_dim,causal,sign", [(128, False, 1), (128, True, 1), (64, False, 1),
+                                                   (256, True, 1), (128, False, -1)],
+                         ids=["d128", "d128_causal", "d64", "d256_causal", "d128_neg_scale"])
+def test_scores_growing_across_key_blocks(head_dim, causal, sign):
+    # Even rows' scores grow with the key index: key j scores ~ j (times the
+    # sign of the scale), i.e. by 11-23 log2 units per 128-key block, above
+    # the 8-unit lazy-rescale threshold.  After a row's first block the kernel
+    # exponentiates against the reference in use; here the row sums overflow
+    # 2^8 on every block, so the block max is found, the reference moves and
+    # the pass is redone, for half the rows of every warp (odd rows have
+    # ordinary scores and keep theirs).
+    from dataclasses import replace
+    n = 1000
+    w = wl.dense(f"growing_d{head_dim}", 1, n, 2, head_dim=head_dim, causal=causal,
+                 scale=sign / float(np.sqrt(head_dim)))
+    inp = wl.make_inputs(w, seed=7)
+    q, k = inp.q.float(), inp.k.float()
+    q[0::2, :, 0] = 4.0 * sign
+    q[1::2, :, 0] = 0.0
+    k[:, :, 0] = torch.arange(n, dtype=torch.float32)[:, None] * 0.25
+    check_full(replace(inp, q=q.to(torch.bfloat16), k=k.to(torch.bfloat16)))
+
+
 # ---------------------------------------------------------------- large index ranges
 def test_many_tiny_sequences_full():
     # 3000 sequences of 0-5 tokens: a large grid.z, empty and one-row docs
