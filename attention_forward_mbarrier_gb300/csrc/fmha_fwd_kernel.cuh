@@ -830,17 +830,25 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         alpha = (m_ref == m_used) ? 1.f : ptx::ex2_approx((m_used - m_ref) * c);
         row_sum = exp_pass_split<kSplit>(s, c, m_ref, t_s, rescale_o, signal_part);
       } else {
-        // head_dim 64: both passes inlined (measured faster there); else one copy
-        constexpr int kPassUnroll = HD == 64 ? 2 : 1;
-#pragma unroll kPassUnroll
-        for (int pass = 0; pass < 2; ++pass) {
+        // one exp pass; true when it must be redone against a moved reference
+        auto pass_redo = [&]() -> bool {
           row_sum = exp_pass(s, c, m_ref, t_s);
-          if (!stale || !__any_sync(0xffffffffu, row_sum > sum_limit)) break;
+          if (!stale || !__any_sync(0xffffffffu, row_sum > sum_limit)) return false;
           stale = false;
           const float m_new = lazy_reference(s, neg, m_used, c, p.rescale_threshold);
-          if (!__any_sync(0xffffffffu, m_new != m_used)) break;
+          if (!__any_sync(0xffffffffu, m_new != m_used)) return false;
           m_ref = m_new;
           ptx::tmem_wait_st();  // the first pass's stores land before they are overwritten
+          return true;
+        };
+        if constexpr (HD == 64) {  // both passes inlined (measured faster there)
+#pragma unroll
+          for (int pass = 0; pass < 2; ++pass)
+            if (!pass_redo()) break;
+        } else {  // one copy of the pass
+#pragma unroll 1
+          for (int pass = 0; pass < 2; ++pass)
+            if (!pass_redo()) break;
         }
         // an infinite m_used (nothing visible yet) gives alpha 0 (its O rows and l are still 0)
         alpha = (m_ref == m_used) ? 1.f : ptx::ex2_approx((m_used - m_ref) * c);
