@@ -372,6 +372,49 @@ __device__ __forceinline__ float row_min128(const float (&s)[128]) {
   return ptx::fmin3(fminf(mn[0], mn[1]), mn[2], mn[3]);
 }
 
+// Ring load idx -> (K or V, key block).  Default order: K_0, V_0, K_1, V_1,
+// ...  Double-buffered S (one query tile per CTA), the order the MMA groups
+// read them in: K_0, K_1, V_0, K_2, V_1, K_3, ..., V_(n-2), V_(n-1) (group g
+// issues PV(g - 2) then QK^T(g)).
+template <bool kDoubleS>
+__device__ __forceinline__ void ring_block(int idx, int n_kv, bool& is_v, int& blk) {
+  if constexpr (!kDoubleS) {
+    is_v = idx & 1;
+    blk = idx >> 1;
+  } else {
+    if (idx == 0) {
+      is_v = false;
+      blk = 0;
+    } else if (n_kv == 1) {
+      is_v = true;
+      blk = 0;
+    } else if (idx == 1) {
+      is_v = false;
+      blk = 1;
+    } else if (idx == 2 * n_kv - 1) {
+      is_v = true;
+      blk = n_kv - 1;
+    } else {
+      const int r = idx - 2;
+      is_v = !(r & 1);
+      blk = (r >> 1) + (r & 1) * 2;
+    }
+  }
+}
+
+// The commit after which ring load idx's block has been read for the last
+// time (its slot is free).  Default: K_s by QK^T(s) (step commit s), V_s by
+// PV(s) (step commit s + 1).  Double-buffered S: group commit g follows
+// PV(g - 2) and QK^T(g); K_0 and K_1 are read by groups 0 and 1, V_m and
+// K_(m + 2) by group m + 2.  (Only loads whose slot is reused are asked.)
+template <bool kDoubleS>
+__device__ __forceinline__ int ring_release_commit(int idx) {
+  if constexpr (!kDoubleS)
+    return (idx >> 1) + (idx & 1);
+  else
+    return idx < 2 ? idx : (idx >> 1) + 1;
+}
+
 // The lazy-rescale reference for a block: its row max (min for a negative
 // scale) replaces the reference in use m_used only when the scaled extreme
 // grew by more than `threshold` (log2 units); NaN while both are the mask
@@ -588,6 +631,10 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
   constexpr uint32_t kTileBytes = D::kTileBytes;
   constexpr uint32_t kOffQ = D::kOffQ, kOffKV = D::kOffKV, kOffBar = D::kOffBar, kOffMisc = D::kOffMisc;
   constexpr uint64_t kSlotDescStep = kTileBytes >> 4;
+  // one query tile per CTA (head_dim 256): two S buffers, so that the next
+  // block's QK^T runs during this block's softmax
+  constexpr bool kDoubleS = D::kTiles == 1;
+  static_assert(!kDoubleS || (kSplit == 4 && D::kStages == 2), "double-buffered S: one P hand-off, two ring slots");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -697,8 +744,11 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       }
     }
     ptx::mbar_arrive_expect_tx(bar, kTileBytes);
-    const CUtensorMap* m = (idx & 1) ? &p.tmap_v : &p.tmap_k;
-    const int y = k0 + kBlockN * (idx >> 1);
+    bool is_v;
+    int blk;
+    ring_block<kDoubleS>(idx, n_kv, is_v, blk);
+    const CUtensorMap* m = is_v ? &p.tmap_v : &p.tmap_k;
+    const int y = k0 + kBlockN * blk;
 #pragma unroll
     for (int hf = 0; hf < D::kHalves; ++hf) ptx::tma_load_2d(dst + hf * kHalfBytes, m, bar, xkv + 64 * hf, y, pol);
   };
@@ -774,8 +824,10 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       const bool tr = (r == 0 && j < kTrMaxBlocks);
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 0);
       ptx::tc_fence_after();
+      // this block's S buffer (two alternate with one query tile per CTA)
+      const uint32_t t_sj = kDoubleS ? t_s + col_s(j & 1) : t_s;
       float s[128];
-      ptx::tmem_ld128_wait(t_s, s);
+      ptx::tmem_ld128_wait(t_sj, s);
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 1);
       const int c0 = j * kBlockN;
       if (tile_key_end - c0 < kBlockN) {  // block crosses the diagonal or the key tail
@@ -802,6 +854,12 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       // a split hand-off, the first one: hence the rescale before that signal).
       auto rescale_o = [&]() {
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if constexpr (kDoubleS) {
+            // PV(j - 1) may still run (S(j) came from group j, before it):
+            // group commit j + 1 follows it
+            if (!wait_bar_warp(ctx, kBarStepDone + ((j + 1) & 1), ((j + 1) >> 1) & 1, kRoleSoftmax)) return;
+            ptx::tc_fence_after();
+          }
           const uint32_t t_o = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16) + col_o(t);
 #pragma unroll
           for (int cc = 0; cc < HD / 32; ++cc) {
@@ -821,18 +879,18 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       };
       if constexpr (kFp8 && kSplit < 4) {
         alpha = (m_ref == m_used) ? 1.f : ptx::ex2_approx((m_used - m_ref) * c);
-        row_sum = exp_pass_fp8_split<kSplit>(s, c, m_ref, t_s, rescale_o, signal_part);
+        row_sum = exp_pass_fp8_split<kSplit>(s, c, m_ref, t_sj, rescale_o, signal_part);
       } else if constexpr (kFp8) {
         alpha = (m_ref == m_used) ? 1.f : ptx::ex2_approx((m_used - m_ref) * c);
-        row_sum = exp_pass_fp8(s, c, m_ref, t_s);
+        row_sum = exp_pass_fp8(s, c, m_ref, t_sj);
         rescale_o();
       } else if constexpr (kSplit < 4) {
         alpha = (m_ref == m_used) ? 1.f : ptx::ex2_approx((m_used - m_ref) * c);
-        row_sum = exp_pass_split<kSplit>(s, c, m_ref, t_s, rescale_o, signal_part);
+        row_sum = exp_pass_split<kSplit>(s, c, m_ref, t_sj, rescale_o, signal_part);
       } else {
         // one exp pass; true when it must be redone against a moved reference
         auto pass_redo = [&]() -> bool {
-          row_sum = exp_pass(s, c, m_ref, t_s);
+          row_sum = exp_pass(s, c, m_ref, t_sj);
           if (!stale || !__any_sync(0xffffffffu, row_sum > sum_limit)) return false;
           stale = false;
           const float m_new = lazy_reference(s, neg, m_used, c, p.rescale_threshold);
@@ -860,7 +918,9 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVReady + t));
+      // (double-buffered S: the softmax can be two blocks ahead of the PVs,
+      // so P hand-offs alternate between the two barriers)
+      if (lane == 0) ptx::mbar_arrive(ctx.bar(kBarPVReady + (kDoubleS ? (j & 1) : t)));
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 4);
       // the other three warps of the warpgroup stamp their own hand-off (skew)
       if (lane == 0 && (warp & 3) != 0 && j < kTrMaxBlocks) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 4 + (warp & 3));
@@ -972,7 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           // of step commit n: K_s by QK^T(s) (commit s), V_s by PV(s) (commit s + 1);
           // the first kStages loads find their slots empty
           const int prev = idx - kStages;
-          const int n = (prev >> 1) + (prev & 1);
+          const int n = ring_release_commit<kDoubleS>(prev);
           if (prev >= 0 && !wait_bar(ctx, kBarStepDone + (n & 1), (n >> 1) & 1, kRoleLoad)) break;
           if (idx < 400) FMHA_TRACE_AT(kTrLoad + idx);
           load_kv(idx, pol_kv);
@@ -998,8 +1058,44 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         const uint64_t kv_desc_mn = desc_mnmajor(base + kOffKV);
         bool issued_any = false;
         bool ok = true;
-        if (n_kv > 0) ok = wait_bar(ctx, kBarKVFull + 0, 0, kRoleMma);
-        if (ok && n_kv > 0) {
+        if constexpr (kDoubleS) {
+          // Group g (0 .. n_kv + 1): PV(g - 2) reading P from S buffer g % 2,
+          // then QK^T(g) into the same buffer, then group commit g (S(g)
+          // ready; ring slots of V_(g-2) and K_g free once it completes).
+          // Block j's softmax thus overlaps QK^T(j + 1) and PV(j - 1).  P(m)
+          // arrives on PVReady[m % 2] (phase m / 2): the softmax may run two
+          // blocks ahead of the PVs.
+          if (n_kv > 0) ok = wait_bar(ctx, kBarQFull + 0, 0, kRoleMma);
+          for (int g = 0; ok && n_kv > 0 && g < n_kv + 2; ++g) {
+            if (g >= 2) {
+              const int m = g - 2;
+              const int vidx = m < n_kv - 1 ? 2 + 2 * m : (n_kv == 1 ? 1 : 2 * n_kv - 1);
+              if (!wait_bar(ctx, kBarKVFull + vidx % kStages, (vidx / kStages) & 1, kRoleMma) ||
+                  !wait_bar(ctx, kBarPVReady + (m & 1), (m >> 1) & 1, kRoleMma)) {
+                ok = false;
+                break;
+              }
+              if (m < kTrMaxBlocks) FMHA_TRACE_AT(kTrMma + m * 8 + 1);
+              ptx::tc_fence_after();
+              issue_pv<HD>(tmem + col_o(0), tmem + col_s(m & 1), kv_desc_mn + kSlotDescStep * (vidx % kStages), m > 0);
+              if (m == n_kv - 1) ptx::mma_commit(ctx.bar(kBarOFinal + 0));
+            }
+            if (g < n_kv) {
+              const int kidx = g < 2 ? g : 2 * g - 1;
+              if (!wait_bar(ctx, kBarKVFull + kidx % kStages, (kidx / kStages) & 1, kRoleMma)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              issue_qk<HD>(tmem + col_s(g & 1), q_desc[0], kv_desc + kSlotDescStep * (kidx % kStages));
+              issued_any = true;
+            }
+            ptx::mma_commit(ctx.bar(kBarStepDone + (g & 1)));
+          }
+        } else if (n_kv > 0) {
+          ok = wait_bar(ctx, kBarKVFull + 0, 0, kRoleMma);
+        }
+        if (!kDoubleS && ok && n_kv > 0) {
           // each tile's first QK^T as soon as its own Q tile has landed
 #pragma unroll
           for (int t = 0; t < kTiles; ++t) {

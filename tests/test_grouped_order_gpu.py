@@ -72,3 +72,28 @@ def test_grouped_order_full(group_lib, w):
     compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
     out_plain, lse_plain = run_gpu(inp)
     assert torch.equal(out, out_plain) and torch.equal(lse, lse_plain)
+
+
+def test_grouped_order_growing_scores(group_lib):
+    # The head-grouped kernel through the softmax's redo path: even rows'
+    # scores grow by ~17 log2 units per 128-key block (see
+    # test_parity_gpu.test_scores_growing_across_key_blocks)
+    from dataclasses import replace
+
+    import numpy as np
+
+    n = 1000
+    w = wl.dense("grp_growing_h6", 1, n, 6, causal=True)
+    inp = wl.make_inputs(w, seed=43)
+    q, k = inp.q.float(), inp.k.float()
+    q[0::2, :, 0] = 4.0
+    q[1::2, :, 0] = 0.0
+    k[:, :, 0] = torch.arange(n, dtype=torch.float32)[:, None] * 0.25
+    inp = replace(inp, q=q.to(torch.bfloat16), k=k.to(torch.bfloat16))
+    assert w.n_kv_heads * w.max_seqlen_k * w.head_dim * 4 > THRESHOLD and w.heads > 4
+    out, lse = run_gpu(inp, library=group_lib)
+    ref_o, ref_l = oracle.oracle_fwd(*inp.oracle_args())
+    compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
+    out_plain, lse_plain = run_gpu(inp)
+    assert torch.equal(out, out_plain) and torch.equal(lse, lse_plain)
+    assert np.isfinite(out.float().cpu().numpy()).all()
