@@ -96,6 +96,9 @@ constexpr int kBarPVReady = 9;   // [2]  P of tile t stored (and its O rows resc
 constexpr int kBarOFinal = 11;   // [2]  last PV of tile t complete
 constexpr int kBarMmaDone = 13;  //      every MMA retired
 constexpr int kBarPVPart = 14;   // [2]  first part of P of tile t stored (split hand-off only)
+// one query tile per CTA (two ring slots): V_m's slot free after PV(m), on the
+// ring barriers the two-slot ring leaves unused
+constexpr int kBarVFree = kBarKVFull + 2;  // [2]
 static_assert(kBarPVPart + 2 == static_cast<int>(kNumBars), "ids");
 
 // P hand-off split ("Kernel Bottleneck Tuning", section "5. Tune the
@@ -402,17 +405,24 @@ __device__ __forceinline__ void ring_block(int idx, int n_kv, bool& is_v, int& b
   }
 }
 
-// The commit after which ring load idx's block has been read for the last
-// time (its slot is free).  Default: K_s by QK^T(s) (step commit s), V_s by
-// PV(s) (step commit s + 1).  Double-buffered S: group commit g follows
-// PV(g - 2) and QK^T(g); K_0 and K_1 are read by groups 0 and 1, V_m and
-// K_(m + 2) by group m + 2.  (Only loads whose slot is reused are asked.)
+// The barrier and phase parity of the commit after which ring load idx's
+// block has been read for the last time (its slot is free).  Default: K_s by
+// QK^T(s) (step commit s), V_s by PV(s) (step commit s + 1), step commit n on
+// StepDone[n % 2].  Double-buffered S: K_g by the commit after QK^T(g)
+// (StepDone[g % 2]), V_m by the commit after PV(m) (VFree[m % 2]).
 template <bool kDoubleS>
-__device__ __forceinline__ int ring_release_commit(int idx) {
-  if constexpr (!kDoubleS)
-    return (idx >> 1) + (idx & 1);
-  else
-    return idx < 2 ? idx : (idx >> 1) + 1;
+__device__ __forceinline__ void ring_release(int idx, int n_kv, int& bar, uint32_t& parity) {
+  if constexpr (!kDoubleS) {
+    const int n = (idx >> 1) + (idx & 1);
+    bar = kBarStepDone + (n & 1);
+    parity = static_cast<uint32_t>(n >> 1) & 1u;
+  } else {
+    bool is_v;
+    int blk;
+    ring_block<true>(idx, n_kv, is_v, blk);
+    bar = (is_v ? kBarVFree : kBarStepDone) + (blk & 1);
+    parity = static_cast<uint32_t>(blk >> 1) & 1u;
+  }
 }
 
 // The lazy-rescale reference for a block: its row max (min for a negative
@@ -855,9 +865,8 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       auto rescale_o = [&]() {
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           if constexpr (kDoubleS) {
-            // PV(j - 1) may still run (S(j) came from group j, before it):
-            // group commit j + 1 follows it
-            if (!wait_bar_warp(ctx, kBarStepDone + ((j + 1) & 1), ((j + 1) >> 1) & 1, kRoleSoftmax)) return;
+            // PV(j - 1) may still run (S(j) came from group j, before it)
+            if (!wait_bar_warp(ctx, kBarVFree + ((j - 1) & 1), ((j - 1) >> 1) & 1, kRoleSoftmax)) return;
             ptx::tc_fence_after();
           }
           const uint32_t t_o = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16) + col_o(t);
@@ -1032,8 +1041,12 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
           // of step commit n: K_s by QK^T(s) (commit s), V_s by PV(s) (commit s + 1);
           // the first kStages loads find their slots empty
           const int prev = idx - kStages;
-          const int n = ring_release_commit<kDoubleS>(prev);
-          if (prev >= 0 && !wait_bar(ctx, kBarStepDone + (n & 1), (n >> 1) & 1, kRoleLoad)) break;
+          if (prev >= 0) {
+            int rel_bar;
+            uint32_t rel_parity;
+            ring_release<kDoubleS>(prev, n_kv, rel_bar, rel_parity);
+            if (!wait_bar(ctx, rel_bar, rel_parity, kRoleLoad)) break;
+          }
           if (idx < 400) FMHA_TRACE_AT(kTrLoad + idx);
           load_kv(idx, pol_kv);
           ++issued;
@@ -1060,11 +1073,13 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
         bool ok = true;
         if constexpr (kDoubleS) {
           // Group g (0 .. n_kv + 1): PV(g - 2) reading P from S buffer g % 2,
-          // then QK^T(g) into the same buffer, then group commit g (S(g)
-          // ready; ring slots of V_(g-2) and K_g free once it completes).
-          // Block j's softmax thus overlaps QK^T(j + 1) and PV(j - 1).  P(m)
-          // arrives on PVReady[m % 2] (phase m / 2): the softmax may run two
-          // blocks ahead of the PVs.
+          // then QK^T(g) into the same buffer; a commit after each (VFree:
+          // V's slot free and O updated; StepDone: S(g) ready, K_g's slot
+          // free), so that a slot is refilled as soon as its reader is done
+          // and the next block's copy runs behind the other MMA.  Block j's
+          // softmax overlaps QK^T(j + 1) and PV(j - 1).  P(m) arrives on
+          // PVReady[m % 2] (phase m / 2): the softmax may run two blocks
+          // ahead of the PVs.
           if (n_kv > 0) ok = wait_bar(ctx, kBarQFull + 0, 0, kRoleMma);
           for (int g = 0; ok && n_kv > 0 && g < n_kv + 2; ++g) {
             if (g >= 2) {
@@ -1078,6 +1093,7 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
               if (m < kTrMaxBlocks) FMHA_TRACE_AT(kTrMma + m * 8 + 1);
               ptx::tc_fence_after();
               issue_pv<HD>(tmem + col_o(0), tmem + col_s(m & 1), kv_desc_mn + kSlotDescStep * (vidx % kStages), m > 0);
+              ptx::mma_commit(ctx.bar(kBarVFree + (m & 1)));  // V_m's slot free, O has PV(m)
               if (m == n_kv - 1) ptx::mma_commit(ctx.bar(kBarOFinal + 0));
             }
             if (g < n_kv) {
@@ -1089,8 +1105,8 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
               ptx::tc_fence_after();
               issue_qk<HD>(tmem + col_s(g & 1), q_desc[0], kv_desc + kSlotDescStep * (kidx % kStages));
               issued_any = true;
+              ptx::mma_commit(ctx.bar(kBarStepDone + (g & 1)));  // S(g) ready, K_g's slot free
             }
-            ptx::mma_commit(ctx.bar(kBarStepDone + (g & 1)));
           }
         } else if (n_kv > 0) {
           ok = wait_bar(ctx, kBarKVFull + 0, 0, kRoleMma);

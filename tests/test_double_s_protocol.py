@@ -4,13 +4,14 @@ run on the CPU.
 With one 128-row query tile per CTA the kernel keeps two S buffers in tensor
 memory (attention_forward_mbarrier_gb300/csrc/fmha_fwd_kernel.cuh, the
 double-buffered S schedule): the MMA thread issues groups g = 0 .. n + 1 of
-PV(g - 2) (P from S buffer g % 2) then QK^T(g) (into the same buffer), one
-commit per group on StepDone[g % 2]; the producer loads the ring in the order
-the groups read it (K_0, K_1, V_0, K_2, V_1, ..., V_(n-2), V_(n-1)) into two
-slots, refilling a slot after the commit of the group that read it; the four
-softmax warps take S(j) from commit j, may rescale O after commit j + 1 (PV
-(j - 1) may still run when S(j) is ready), and hand P(j) off on PVReady[j % 2]
-because they can run two blocks ahead of the PVs.
+PV(g - 2) (P from S buffer g % 2) then QK^T(g) (into the same buffer), with a
+commit after the PV (VFree[m % 2]: V_m's slot is free) and one after the
+QK^T (StepDone[g % 2]: S(g) ready, K_g's slot free); the producer loads the
+ring in the order the groups read it (K_0, K_1, V_0, K_2, V_1, ..., V_(n-2),
+V_(n-1)) into two slots, refilling a slot after the commit that frees it; the
+four softmax warps take S(j) from StepDone, may rescale O once PV(j - 1) has
+completed (VFree; it may still run when S(j) is ready), and hand P(j) off on
+PVReady[j % 2] because they can run two blocks ahead of the PVs.
 
 The model replays those waits and signals under random interleavings, with
 an in-order tensor pipe and copies that land in any order.  Checked on every
@@ -53,9 +54,14 @@ def ring_block(idx, n):
     return ("V", r >> 1) if r % 2 == 0 else ("K", (r >> 1) + 2)
 
 
-def release_commit(idx):
-    """The group commit after which load idx's slot is free."""
-    return idx if idx < 2 else (idx >> 1) + 1
+def release(idx, n):
+    """(barrier, phase) after which load idx's slot is free: K_g by the commit
+    after QK^T(g) (StepDone[g % 2]), V_m by the commit after PV(m)
+    (VFree[m % 2])."""
+    kind, blk = ring_block(idx, n)
+    if kind == "K":
+        return f"SD{blk & 1}", blk >> 1
+    return f"VF{blk & 1}", blk >> 1
 
 
 def simulate(n, seed, p_rescale, p_barriers=2):
@@ -66,7 +72,7 @@ def simulate(n, seed, p_rescale, p_barriers=2):
     def bar(name, count=1):
         bars[name] = Bar(name, count)
 
-    for name in ("QFull", "KV0", "KV1", "SD0", "SD1", "OF"):
+    for name in ("QFull", "KV0", "KV1", "SD0", "SD1", "VF0", "VF1", "OF"):
         bar(name)
     for b in range(p_barriers):
         bar(f"PV{b}", 4)
@@ -94,8 +100,7 @@ def simulate(n, seed, p_rescale, p_barriers=2):
         copies.append(("QFull", lambda: None))
         for idx in range(2 * n):
             if idx >= 2:
-                g = release_commit(idx - 2)
-                yield from wait(f"SD{g & 1}", g >> 1, "producer")
+                yield from wait(*release(idx - 2, n), "producer")
             s = idx % 2
             if st["readers"][s]:
                 problems.append(f"slot {s} refilled while read (load {idx})")
@@ -127,6 +132,7 @@ def simulate(n, seed, p_rescale, p_barriers=2):
                     st["readers"][vs] -= 1
 
                 pipe.append(("mma", pv))
+                pipe.append(("commit", f"VF{m & 1}"))
                 if m == n - 1:
                     pipe.append(("commit", "OF"))
             if g < n:
@@ -144,7 +150,7 @@ def simulate(n, seed, p_rescale, p_barriers=2):
                     st["readers"][ks] -= 1
 
                 pipe.append(("mma", qk))
-            pipe.append(("commit", f"SD{g & 1}"))
+                pipe.append(("commit", f"SD{g & 1}"))
             yield
 
     def softmax(w):
@@ -154,7 +160,7 @@ def simulate(n, seed, p_rescale, p_barriers=2):
                 problems.append(f"softmax {w} reads S {st['S'].get(j % 2)} for block {j}")
             yield
             if j > 0 and rnd.random() < p_rescale:
-                yield from wait(f"SD{(j + 1) & 1}", (j + 1) >> 1, f"softmax {w} rescale")
+                yield from wait(f"VF{(j - 1) & 1}", (j - 1) >> 1, f"softmax {w} rescale")
                 if st["O"] != j - 1:
                     problems.append(f"rescale at block {j} sees O after PV({st['O']})")
                 st["o_busy"] += 1
