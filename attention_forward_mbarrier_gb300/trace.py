@@ -428,7 +428,7 @@ def summarize_backward(a: np.ndarray, bk: np.ndarray) -> dict:
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", default=wl.C2.name, choices=sorted(wl.CONFIGS))
+    ap.add_argument("--workload", default=wl.C2.name, choices=sorted({**wl.CONFIGS, **wl.EXTRA}))
     ap.add_argument("--row", type=int, default=0, help="query block (256 rows) of head 0 to show")
     ap.add_argument("--raw", default=None, help="save the raw stamps (.npy)")
     ap.add_argument("--flags", default="", help="extra -D flags for the trace build (tuning variants)")
@@ -436,7 +436,7 @@ def main():
     ap.add_argument("--persistent", action="store_true", help="trace the persistent variant")
     ap.add_argument("--backward", action="store_true", help="trace the backward pass's dQ and dK/dV kernels")
     args = ap.parse_args()
-    w = wl.CONFIGS[args.workload]
+    w = {**wl.CONFIGS, **wl.EXTRA}[args.workload]
     if args.backward:
         a, bk = run_backward(w, flags=args.flags.split())
         print(json.dumps({"workload": w.name, "flags": args.flags, "backward": summarize_backward(a, bk)}, indent=1))
