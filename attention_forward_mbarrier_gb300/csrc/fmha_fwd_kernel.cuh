@@ -859,9 +859,10 @@ __global__ void __launch_bounds__(kThreads, 1) fmha_fwd_kernel(const __grid_cons
       float m_ref = stale ? m_used : lazy_reference(s, neg, m_used, c, p.rescale_threshold);
       if (tr) FMHA_TRACE_AT(kTrSoftmax + t * 512 + j * 8 + 2);
       float alpha = 1.f;
-      // Rescale this warp's O rows.  PV_t(j-1) has completed (S_t(j) is
-      // committed after it) and PV_t(j) waits for this warp's P hand-off (with
-      // a split hand-off, the first one: hence the rescale before that signal).
+      // Rescale this warp's O rows.  PV_t(j-1) has completed (two tiles: S_t(j)
+      // is committed after it; one tile with two S buffers: waited for below)
+      // and PV_t(j) waits for this warp's P hand-off (with a split hand-off,
+      // the first one: hence the rescale before that signal).
       auto rescale_o = [&]() {
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           if constexpr (kDoubleS) {
